@@ -1,0 +1,142 @@
+/*
+ * mla_paged.h -- C ABI of the GB300 (sm_103a) paged Multi-head Latent Attention library.
+ *
+ * What the calls compute (flashinfer-bench "MLA Paged", sections "decode" and
+ * "prefill"): for every query row r and query head h,
+ *
+ *   s_t      = sm_scale * (q_nope[r,h,:] . ckv[t,:] + q_pe[r,h,:] . kpe[t,:])
+ *   lse[r,h] = log(sum_t exp(s_t))                       (natural log)
+ *   out[r,h] = sum_t exp(s_t - lse[r,h]) * ckv[t,:]      (V is the 512-wide latent itself,
+ *                                                         Modular MAX "mla_decoding_single_batch")
+ *
+ * where t runs over the key slots kv_indices[kv_indptr[b] .. kv_indptr[b+1]) of the
+ * row's request b (decode), or over the first kv_len_b - q_len_b + i + 1 of them for
+ * query i of request b (prefill: causal, bottom-right aligned).  One KV head is shared
+ * by all query heads.
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers to contiguous row-major arrays; the
+ *    caller owns every buffer (inputs, outputs, workspace).  The library allocates
+ *    nothing on the device and keeps only a host-side cache of TMA descriptors keyed
+ *    by pointer and shape.
+ *  - bf16 tensors (q_nope, q_pe, ckv_cache, kpe_cache, out) must start on a 16-byte
+ *    boundary (TMA requirement) or the call returns MLA_ERR_ALIGN.
+ *  - kv_indices holds token slots: slot = page * page_size + offset, an index into the
+ *    caches viewed as [num_pages * page_size, 512] and [.., 64] (the physical-index
+ *    mapping of FlashMLA's abs_indices2indices_in_kvcache).  kv_indptr counts keys, so
+ *    a request's kv length is kv_indptr[b+1] - kv_indptr[b].
+ *  - Calls only enqueue work on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  They never synchronise and never read device memory on the host, so
+ *    they may be captured in a CUDA graph.  Launch errors are returned; faults
+ *    inside a kernel surface at the caller's next synchronisation.
+ *  - Slots outside kv_indices are never read into the result: NaN or Inf there does
+ *    not change the output.  An index outside [0, num_pages*page_size) reads zeros
+ *    (TMA out-of-bounds fill) instead of faulting; MLA_VALIDATE reports it.
+ *  - A request with no keys gets out = 0 and lse = -inf.
+ */
+#ifndef MLA_PAGED_H
+#define MLA_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes (0 = success, negative = error). */
+enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_NULL = -1,       /* a required pointer is NULL                                  */
+  MLA_ERR_DIMS = -2,       /* head dims != 512/64, heads not in 1..128, bad sizes          */
+  MLA_ERR_ALIGN = -3,      /* a bf16 tensor pointer is not 16-byte aligned                 */
+  MLA_ERR_WORKSPACE = -4,  /* workspace NULL or smaller than mla_workspace_bytes()         */
+  MLA_ERR_LAUNCH = -5,     /* a kernel launch failed (cudaGetLastError after the launch)   */
+  MLA_ERR_BAD_INDEX = -6,  /* (device status) MLA_VALIDATE found bad indptr/indices        */
+  MLA_ERR_TIMEOUT = -7,    /* (device status) a bounded wait inside a kernel gave up       */
+  MLA_ERR_CUDA = -8,       /* a CUDA runtime/driver call failed (device query, TMA encode) */
+  MLA_ERR_UNSUPPORTED = -9 /* no sm_103a-class device is current                           */
+};
+
+/* Flags (bitwise OR). */
+enum mla_flags {
+  MLA_VALIDATE = 1 /* run an index-validation kernel first; it records MLA_ERR_BAD_INDEX in
+                      the workspace status word (read it with mla_read_device_status) */
+};
+
+/* Problem sizes.  All fields are host-side values. */
+typedef struct mla_dims {
+  int32_t batch;          /* decode: number of requests (= query rows); prefill: requests   */
+  int32_t num_qo_heads;   /* query heads, 1..128 (one shared KV head)                       */
+  int32_t head_dim_ckv;   /* must be 512                                                     */
+  int32_t head_dim_kpe;   /* must be 64                                                      */
+  int32_t num_pages;      /* pages in ckv_cache / kpe_cache                                  */
+  int32_t page_size;      /* slots per page (>= 1); num_pages * page_size < 2^31             */
+  int32_t total_q;        /* prefill: qo_indptr[batch] (query rows); decode: ignored         */
+  int32_t num_kv_indices; /* kv_indptr[batch]: length of kv_indices                          */
+  int32_t num_workers;    /* split-KV workers (CTA pairs); 0 = one per SM pair of the device */
+} mla_dims;
+
+/*
+ * Paged MLA decode: flashinfer-bench "MLA Paged", section "decode".
+ *   q_nope     [batch, H, 512] bf16      q_pe      [batch, H, 64] bf16
+ *   ckv_cache  [num_pages, page_size, 512] bf16
+ *   kpe_cache  [num_pages, page_size, 64]  bf16
+ *   kv_indptr  [batch + 1] int32 (non-decreasing, kv_indptr[0] = 0)
+ *   kv_indices [num_kv_indices] int32 token slots
+ *   sm_scale   softmax scale multiplying the q.k dot product
+ *   out        [batch, H, 512] bf16 (written)   lse [batch, H] fp32, natural log (written)
+ *   workspace  device scratch of at least mla_workspace_bytes(dims, 0) bytes, caller-owned;
+ *              it holds split-KV partial results and the device status word.  Calls that
+ *              share a workspace must not overlap on the GPU.
+ *   flags      MLA_VALIDATE or 0;  stream: cudaStream_t
+ * Returns MLA_OK or a negative mla_status; nothing is launched on an argument error.
+ */
+int mla_paged_decode(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                     const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     float sm_scale, void* out, float* lse, const mla_dims* dims,
+                     void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
+ * Paged MLA causal prefill: flashinfer-bench "MLA Paged", section "prefill"; the
+ * causal mask is bottom-right aligned: query i of request b sees its first
+ * kv_len_b - q_len_b + i + 1 keys (kv_len_b >= q_len_b is required; rows that
+ * would see no key get out = 0, lse = -inf, and MLA_VALIDATE flags them).
+ *   q_nope [total_q, H, 512], q_pe [total_q, H, 64], out [total_q, H, 512], lse [total_q, H]
+ *   qo_indptr [batch + 1] int32 query offsets (qo_indptr[batch] = total_q)
+ *   other arguments as for mla_paged_decode; workspace >= mla_workspace_bytes(dims, 1).
+ */
+int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                      const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, float sm_scale, void* out, float* lse,
+                      const mla_dims* dims, void* workspace, size_t workspace_bytes, int flags,
+                      void* stream);
+
+/* Workspace bytes a call with these dims needs (0 on invalid dims).  With
+ * dims->num_workers == 0 it queries the current device's SM count. */
+size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill);
+
+/* Number of split-KV workers (CTA pairs) used when dims->num_workers == 0, for the
+ * current device; negative mla_status on failure. */
+int mla_default_num_workers(void);
+
+/* Human-readable name of a status code (static string). */
+const char* mla_status_string(int status);
+
+/* Synchronises `stream`, reads the device status word kept in `workspace` (MLA_OK,
+ * MLA_ERR_BAD_INDEX or MLA_ERR_TIMEOUT), clears it, and returns it.  Returns
+ * MLA_ERR_CUDA if the synchronisation itself reports an error. */
+int mla_read_device_status(void* workspace, void* stream);
+
+/* Kernel timing for benchmarks.  When enabled, every call records CUDA events on its
+ * stream around its main attention kernel and its combine kernel;
+ * mla_profile_read synchronises on the last events, returns the summed milliseconds
+ * and the number of timed calls since the last read, and resets the sums. */
+int mla_profile_enable(int on);
+int mla_profile_read(double* main_ms, double* combine_ms, int* calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_PAGED_H */

@@ -1,0 +1,221 @@
+"""Python binding of libmla_paged.so: paged Multi-head Latent Attention on GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the library's CUDA
+kernels, called through its C ABI (include/mla_paged.h).  There is no CPU path: if the
+library is missing or the tensors are not on a CUDA device, the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+from . import _build
+
+HEAD_DIM_CKV = 512
+HEAD_DIM_KPE = 64
+MLA_VALIDATE = 1
+
+_STATUS = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_DIMS", -3: "MLA_ERR_ALIGN",
+           -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_LAUNCH", -6: "MLA_ERR_BAD_INDEX",
+           -7: "MLA_ERR_TIMEOUT", -8: "MLA_ERR_CUDA", -9: "MLA_ERR_UNSUPPORTED"}
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {string_of(status)} ({status})")
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_qo_heads", ctypes.c_int32),
+                ("head_dim_ckv", ctypes.c_int32), ("head_dim_kpe", ctypes.c_int32),
+                ("num_pages", ctypes.c_int32), ("page_size", ctypes.c_int32),
+                ("total_q", ctypes.c_int32), ("num_kv_indices", ctypes.c_int32),
+                ("num_workers", ctypes.c_int32)]
+
+
+_lib = None
+
+# (name, restype, argtypes) of every symbol declared in include/mla_paged.h
+_P = ctypes.c_void_p
+_SIGNATURES = [
+    ("mla_paged_decode", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
+      ctypes.c_int, _P]),
+    ("mla_paged_prefill", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
+      ctypes.c_int, _P]),
+    ("mla_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
+    ("mla_default_num_workers", ctypes.c_int, []),
+    ("mla_status_string", ctypes.c_char_p, [ctypes.c_int]),
+    ("mla_read_device_status", ctypes.c_int, [_P, _P]),
+    ("mla_profile_enable", ctypes.c_int, [ctypes.c_int]),
+    ("mla_profile_read", ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                                        ctypes.POINTER(ctypes.c_int)]),
+]
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load the library (it must have been built: ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build it first (python -m paged_head_latent_gb300._build)")
+        l = ctypes.CDLL(path)
+        for name, res, args in _SIGNATURES:
+            f = getattr(l, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def string_of(status: int) -> str:
+    try:
+        return lib().mla_status_string(status).decode()
+    except Exception:
+        return _STATUS.get(status, "unknown")
+
+
+def make_dims(batch, num_qo_heads, num_pages, page_size, num_kv_indices, total_q=0, num_workers=0):
+    return MlaDims(batch, num_qo_heads, HEAD_DIM_CKV, HEAD_DIM_KPE, num_pages, page_size, total_q,
+                   num_kv_indices, num_workers)
+
+
+def workspace_bytes(dims: MlaDims, is_prefill: bool) -> int:
+    return int(lib().mla_workspace_bytes(ctypes.byref(dims), 1 if is_prefill else 0))
+
+
+def default_num_workers() -> int:
+    n = lib().mla_default_num_workers()
+    if n < 0:
+        raise MlaError(n, "mla_default_num_workers")
+    return n
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check_cuda(name, t, dtype):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (there is no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _cache_geometry(ckv_cache, kpe_cache):
+    if ckv_cache.dim() != 3 or ckv_cache.shape[-1] != HEAD_DIM_CKV:
+        raise ValueError("ckv_cache must be [num_pages, page_size, 512]")
+    if kpe_cache.shape != (ckv_cache.shape[0], ckv_cache.shape[1], HEAD_DIM_KPE):
+        raise ValueError("kpe_cache must be [num_pages, page_size, 64] matching ckv_cache")
+    return ckv_cache.shape[0], ckv_cache.shape[1]
+
+
+def _call(prefill, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
+          out, lse, workspace, flags, num_workers, stream):
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache), ("kpe_cache", kpe_cache)):
+        _check_cuda(n, t, torch.bfloat16)
+    for n, t in (("kv_indptr", kv_indptr), ("kv_indices", kv_indices)) + (
+            (("qo_indptr", qo_indptr),) if prefill else ()):
+        _check_cuda(n, t, torch.int32)
+    rows, heads = q_nope.shape[0], q_nope.shape[1]
+    if q_nope.shape != (rows, heads, HEAD_DIM_CKV) or q_pe.shape != (rows, heads, HEAD_DIM_KPE):
+        raise ValueError("q_nope must be [rows, H, 512] and q_pe [rows, H, 64]")
+    num_pages, page_size = _cache_geometry(ckv_cache, kpe_cache)
+    batch = kv_indptr.numel() - 1
+    if prefill and qo_indptr.numel() != batch + 1:
+        raise ValueError("qo_indptr and kv_indptr must both have batch + 1 entries")
+    if not prefill and rows != batch:
+        raise ValueError("decode: q_nope.shape[0] must equal len(kv_indptr) - 1")
+    dims = make_dims(batch, heads, num_pages, page_size, kv_indices.numel(),
+                     total_q=rows if prefill else 0, num_workers=num_workers)
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty(rows, heads, HEAD_DIM_CKV, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=dev)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("lse", lse, torch.float32)
+    if out.shape != (rows, heads, HEAD_DIM_CKV) or lse.shape != (rows, heads):
+        raise ValueError("out must be [rows, H, 512] and lse [rows, H]")
+    need = workspace_bytes(dims, prefill)
+    if need == 0:
+        raise MlaError(-2, "mla_workspace_bytes")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.device(dev):
+        if prefill:
+            st = lib().mla_paged_prefill(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                         _ptr(qo_indptr), _ptr(kv_indptr), _ptr(kv_indices),
+                                         float(sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                         _ptr(workspace), workspace.numel(), int(flags), sp)
+        else:
+            st = lib().mla_paged_decode(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                        _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out),
+                                        _ptr(lse), ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                        int(flags), sp)
+    if st != 0:
+        raise MlaError(st, "mla_paged_prefill" if prefill else "mla_paged_decode")
+    return out, lse
+
+
+def mla_paged_decode(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale,
+                     out=None, lse=None, workspace=None, flags=0, num_workers=0,
+                     stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA decode (flashinfer-bench "MLA Paged", section "decode").  Returns (out, lse)."""
+    return _call(False, q_nope, q_pe, ckv_cache, kpe_cache, None, kv_indptr, kv_indices, sm_scale,
+                 out, lse, workspace, flags, num_workers, stream)
+
+
+def mla_paged_prefill(q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
+                      out=None, lse=None, workspace=None, flags=0, num_workers=0,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA causal prefill, bottom-right aligned ("MLA Paged", section "prefill")."""
+    return _call(True, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
+                 out, lse, workspace, flags, num_workers, stream)
+
+
+def read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    """Synchronise, read and clear the device status word in ``workspace``."""
+    if stream is None:
+        stream = torch.cuda.current_stream(workspace.device)
+    return int(lib().mla_read_device_status(_ptr(workspace), ctypes.c_void_p(stream.cuda_stream)))
+
+
+def profile_enable(on: bool = True) -> None:
+    lib().mla_profile_enable(1 if on else 0)
+
+
+def profile_read():
+    """(main-kernel ms, combine ms, timed calls) since the last read."""
+    a, b, n = ctypes.c_double(), ctypes.c_double(), ctypes.c_int()
+    st = lib().mla_profile_read(ctypes.byref(a), ctypes.byref(b), ctypes.byref(n))
+    if st != 0:
+        raise MlaError(st, "mla_profile_read")
+    return a.value, b.value, n.value
+
+
+def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, stream=None):
+    """Call decode or prefill on a ``workloads.Workload`` whose tensors are on the GPU."""
+    if w.kind == "decode":
+        return mla_paged_decode(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices,
+                                w.sm_scale, out, lse, workspace, flags, num_workers, stream)
+    return mla_paged_prefill(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.qo_indptr, w.kv_indptr,
+                             w.kv_indices, w.sm_scale, out, lse, workspace, flags, num_workers, stream)

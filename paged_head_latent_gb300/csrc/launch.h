@@ -1,0 +1,17 @@
+// launch.h -- host-side launchers, one per kernel translation unit.
+#pragma once
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace mla {
+
+// The attention kernel over all workers: writes whole rows to out/lse and split
+// rows' fragments to the workspace, plus each worker's combine record.
+cudaError_t launch_attention(const MlaParams& p, cudaStream_t stream);
+// Merge of split rows' fragments (one CTA per worker and head).
+cudaError_t launch_combine(const MlaParams& p, cudaStream_t stream);
+// Optional index validation (sets the status word; never traps).
+cudaError_t launch_validate(const MlaParams& p, cudaStream_t stream);
+
+}  // namespace mla

@@ -1,0 +1,259 @@
+// mla_api.cu -- the C ABI: argument checks, workspace layout, kernel launches.
+//
+// Every entry point only enqueues work on the caller's stream; nothing here
+// synchronises or reads device memory except mla_read_device_status and
+// mla_profile_read, which exist to do exactly that.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <mutex>
+#include <vector>
+
+#include "../../include/mla_paged.h"
+#include "common.cuh"
+#include "launch.h"
+
+namespace {
+
+using mla::MlaParams;
+
+struct DeviceInfo {
+  int sms = 0;
+  int major = 0, minor = 0;
+  bool ok = false;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+int query_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ok) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MLA_ERR_CUDA;
+    }
+    d.ok = true;
+  }
+  *out = d;
+  return MLA_OK;
+}
+
+int check_dims(const mla_dims* d, bool prefill) {
+  if (!d) return MLA_ERR_NULL;
+  if (d->head_dim_ckv != mla::kDimCkv || d->head_dim_kpe != mla::kDimKpe) return MLA_ERR_DIMS;
+  if (d->num_qo_heads < 1 || d->num_qo_heads > mla::kMaxHeads) return MLA_ERR_DIMS;
+  if (d->batch < 0 || d->num_pages < 0 || d->page_size < 1 || d->num_kv_indices < 0) return MLA_ERR_DIMS;
+  if (d->num_workers < 0) return MLA_ERR_DIMS;
+  if ((long long)d->num_pages * d->page_size >= (1LL << 31)) return MLA_ERR_DIMS;
+  if (prefill && d->total_q < 0) return MLA_ERR_DIMS;
+  // Output row count times heads must index within int64 comfortably; rows*H < 2^31.
+  long long rows = prefill ? d->total_q : d->batch;
+  if (rows * d->num_qo_heads >= (1LL << 31)) return MLA_ERR_DIMS;
+  return MLA_OK;
+}
+
+int resolve_workers(const mla_dims* d, int* G) {
+  if (d->num_workers > 0) {
+    *G = d->num_workers;
+    return MLA_OK;
+  }
+  DeviceInfo info;
+  int st = query_device(&info);
+  if (st != MLA_OK) return st;
+  *G = info.sms / 2 > 0 ? info.sms / 2 : 1;
+  return MLA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------- profiling
+struct ProfileState {
+  bool on = false;
+  std::vector<cudaEvent_t> ev;  // 3 per call
+  size_t used = 0;              // triples in use
+};
+ProfileState g_prof;
+
+cudaEvent_t* profile_slot() {
+  if (!g_prof.on) return nullptr;
+  size_t need = (g_prof.used + 1) * 3;
+  while (g_prof.ev.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_prof.ev.push_back(e);
+  }
+  cudaEvent_t* slot = &g_prof.ev[g_prof.used * 3];
+  ++g_prof.used;
+  return slot;
+}
+
+int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cache,
+        const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
+        const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
+        void* workspace, size_t workspace_bytes, int flags, void* stream_ptr) {
+  int st = check_dims(dims, prefill);
+  if (st != MLA_OK) return st;
+  const long long rows = prefill ? dims->total_q : dims->batch;
+  if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indptr || !out || !lse) return MLA_ERR_NULL;
+  if (prefill && !qo_indptr) return MLA_ERR_NULL;
+  if (dims->num_kv_indices > 0 && !kv_indices) return MLA_ERR_NULL;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
+      !aligned16(out))
+    return MLA_ERR_ALIGN;
+  if (!std::isfinite(sm_scale)) return MLA_ERR_DIMS;
+  int G = 0;
+  st = resolve_workers(dims, &G);
+  if (st != MLA_OK) return st;
+  const mla::WorkspaceLayout lay(G, dims->num_qo_heads);
+  if (!workspace || workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MLA_ERR_ALIGN;
+  if (rows == 0) return MLA_OK;
+  DeviceInfo info;
+  st = query_device(&info);
+  if (st != MLA_OK) return st;
+  if (info.major != 10 || info.minor != 3) return MLA_ERR_UNSUPPORTED;
+
+  MlaParams p{};
+  p.q_nope = static_cast<const __nv_bfloat16*>(q_nope);
+  p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  p.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
+  p.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+  p.kv_indptr = kv_indptr;
+  p.qo_indptr = prefill ? qo_indptr : nullptr;
+  p.kv_indices = kv_indices;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.batch = dims->batch;
+  p.heads = dims->num_qo_heads;
+  p.rows = (int)rows;
+  p.num_slots = dims->num_pages * dims->page_size;
+  p.num_kv_indices = dims->num_kv_indices;
+  p.workers = G;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  p.status = reinterpret_cast<uint32_t*>(ws);
+  p.records = reinterpret_cast<mla::CombineRecord*>(ws + lay.records);
+  p.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
+  p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaGetLastError();  // clear stale errors so the checks below see only ours
+  if (flags & MLA_VALIDATE) {
+    if (mla::launch_validate(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  }
+  cudaEvent_t* ev = profile_slot();
+  if (ev) cudaEventRecord(ev[0], stream);
+  if (mla::launch_attention(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (ev) cudaEventRecord(ev[1], stream);
+  if (mla::launch_combine(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (ev) cudaEventRecord(ev[2], stream);
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mla_paged_decode(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                     const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                     float sm_scale, void* out, float* lse, const mla_dims* dims,
+                     void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  return run(false, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, kv_indptr, kv_indices, sm_scale,
+             out, lse, dims, workspace, workspace_bytes, flags, stream);
+}
+
+int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                      const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
+                      const int32_t* kv_indices, float sm_scale, void* out, float* lse,
+                      const mla_dims* dims, void* workspace, size_t workspace_bytes, int flags,
+                      void* stream) {
+  return run(true, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
+             out, lse, dims, workspace, workspace_bytes, flags, stream);
+}
+
+size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill) {
+  if (check_dims(dims, is_prefill != 0) != MLA_OK) return 0;
+  int G = 0;
+  if (resolve_workers(dims, &G) != MLA_OK) return 0;
+  return mla::WorkspaceLayout(G, dims->num_qo_heads).total;
+}
+
+int mla_default_num_workers(void) {
+  DeviceInfo info;
+  int st = query_device(&info);
+  if (st != MLA_OK) return st;
+  return info.sms / 2 > 0 ? info.sms / 2 : 1;
+}
+
+const char* mla_status_string(int status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_NULL: return "MLA_ERR_NULL: a required pointer is NULL";
+    case MLA_ERR_DIMS: return "MLA_ERR_DIMS: unsupported or inconsistent sizes";
+    case MLA_ERR_ALIGN: return "MLA_ERR_ALIGN: a tensor pointer is not 16-byte aligned";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_LAUNCH: return "MLA_ERR_LAUNCH: a kernel launch failed";
+    case MLA_ERR_BAD_INDEX: return "MLA_ERR_BAD_INDEX: indptr/indices failed validation";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait in a kernel gave up";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call failed";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: current device is not sm_103";
+    default: return "unknown mla_status";
+  }
+}
+
+int mla_read_device_status(void* workspace, void* stream_ptr) {
+  if (!workspace) return MLA_ERR_NULL;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MLA_ERR_CUDA;
+  }
+  if (word != 0) {
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+      return MLA_ERR_CUDA;
+  }
+  if (word & mla::kStatusTimeout) return MLA_ERR_TIMEOUT;
+  if (word & mla::kStatusBadIndex) return MLA_ERR_BAD_INDEX;
+  return MLA_OK;
+}
+
+int mla_profile_enable(int on) {
+  g_prof.on = on != 0;
+  g_prof.used = 0;
+  return MLA_OK;
+}
+
+int mla_profile_read(double* main_ms, double* combine_ms, int* calls) {
+  double a = 0, b = 0;
+  for (size_t i = 0; i < g_prof.used; ++i) {
+    cudaEvent_t* e = &g_prof.ev[i * 3];
+    if (cudaEventSynchronize(e[2]) != cudaSuccess) return MLA_ERR_CUDA;
+    float x = 0, y = 0;
+    if (cudaEventElapsedTime(&x, e[0], e[1]) != cudaSuccess ||
+        cudaEventElapsedTime(&y, e[1], e[2]) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    a += x;
+    b += y;
+  }
+  if (main_ms) *main_ms = a;
+  if (combine_ms) *combine_ms = b;
+  if (calls) *calls = (int)g_prof.used;
+  g_prof.used = 0;
+  return MLA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// plan.cuh -- the split-KV partition shared by the attention kernels and the combine.
+//
+// Work is counted in key tiles of kTileKeys keys.  A query row that sees L keys
+// owns ceil(L / kTileKeys) tiles; rows are laid out in order (request by request,
+// query by query) to form one global tile sequence of length T.  Worker w of G
+// (a CTA pair) takes the contiguous range [floor(w*T/G), floor((w+1)*T/G)).  A
+// row cut by a worker boundary is a split row: each worker that touches it writes
+// a partial (normalised output + lse) and the worker holding the row's last tile
+// merges them in the combine kernel, in worker order.
+//
+// This is the split-K partition of the Modular MAX "mla_decoding_single_batch"
+// page (key range split across blocks, with exp-sum / max statistics merged
+// afterwards) computed on the device from kv_indptr / qo_indptr, so that no host
+// planning step (the FlashMLA get_mla_metadata step) is needed and the call can
+// be captured in a CUDA graph.
+#pragma once
+#include <cstdint>
+
+namespace mla {
+
+constexpr int kTileKeys = 64;
+
+// Sum over x = 1..n of ceil(x / 64): the tiles of rows with lengths 1..n.
+__device__ __forceinline__ long long cum_tiles(long long n) {
+  if (n <= 0) return 0;
+  long long a = n / kTileKeys, r = n % kTileKeys;
+  return 32LL * a * (a + 1) + r * (a + 1);
+}
+
+__device__ __forceinline__ int row_tiles(long long len) {
+  return len <= 0 ? 0 : (int)((len + kTileKeys - 1) / kTileKeys);
+}
+
+// Per-request geometry.  Decode is prefill with q_len = 1 and qo = b.
+struct Req {
+  int qo0;      // first query row of the request
+  int q_len;    // query rows
+  int kv0;      // first kv_indices entry of the request
+  int kv_len;   // keys of the request
+};
+
+struct PlanArgs {
+  const int32_t* kv_indptr;
+  const int32_t* qo_indptr;  // nullptr for decode
+  int batch;
+  int num_kv_indices;
+};
+
+__device__ __forceinline__ Req load_req(const PlanArgs& p, int b) {
+  Req r;
+  int k0 = __ldg(p.kv_indptr + b), k1 = __ldg(p.kv_indptr + b + 1);
+  // Clamp so that corrupt indptr never leads to reads outside kv_indices.
+  k0 = min(max(k0, 0), p.num_kv_indices);
+  k1 = min(max(k1, k0), p.num_kv_indices);
+  r.kv0 = k0;
+  r.kv_len = k1 - k0;
+  if (p.qo_indptr) {
+    int q0 = __ldg(p.qo_indptr + b), q1 = __ldg(p.qo_indptr + b + 1);
+    r.qo0 = q0;
+    r.q_len = max(q1 - q0, 0);
+  } else {
+    r.qo0 = b;
+    r.q_len = 1;
+  }
+  return r;
+}
+
+// Keys seen by query i of request r (bottom-right causal; decode: all keys).
+__device__ __forceinline__ long long row_len(const Req& r, int i) {
+  return (long long)r.kv_len - r.q_len + i + 1;
+}
+
+__device__ __forceinline__ long long req_tiles(const Req& r) {
+  long long p = (long long)r.kv_len - r.q_len;
+  return cum_tiles(p + r.q_len) - cum_tiles(p);
+}
+
+// Tiles owned by query rows 0..i-1 of request r.
+__device__ __forceinline__ long long req_tiles_before(const Req& r, int i) {
+  long long p = (long long)r.kv_len - r.q_len;
+  return cum_tiles(p + i) - cum_tiles(p);
+}
+
+// Worker holding global tile t.
+__device__ __forceinline__ int worker_of(long long t, long long T, int G) {
+  return (int)(((t + 1) * (long long)G - 1) / T);
+}
+
+__device__ __forceinline__ long long worker_start(int w, long long T, int G) {
+  return (long long)w * T / G;
+}
+
+// Where a worker starts: request, query row within it, tile within the row.
+struct Cursor {
+  int b;           // request
+  int i;           // query row within the request
+  int t;           // tile within the row
+  long long g;     // global tile index
+  long long tile0; // global index of the request's first tile
+};
+
+// Executed by one full warp.  Returns T (total tiles) and the cursor at global
+// tile `start_of(T)` for worker w.  Cost: two passes over the requests, 32 at a time.
+__device__ inline long long warp_plan(const PlanArgs& p, int w, int G, Cursor* cur) {
+  const int lane = threadIdx.x & 31;
+  long long T = 0;
+  for (int base = 0; base < p.batch; base += 32) {
+    int b = base + lane;
+    long long n = 0;
+    if (b < p.batch) n = req_tiles(load_req(p, b));
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    T += n;
+  }
+  cur->b = p.batch;
+  cur->i = 0;
+  cur->t = 0;
+  cur->g = 0;
+  cur->tile0 = 0;
+  if (T == 0) return 0;
+  const long long s = worker_start(w, T, G);
+  long long run = 0;
+  for (int base = 0; base < p.batch; base += 32) {
+    int b = base + lane;
+    Req r;
+    long long n = 0;
+    if (b < p.batch) {
+      r = load_req(p, b);
+      n = req_tiles(r);
+    }
+    long long incl = n;
+    for (int o = 1; o < 32; o <<= 1) {
+      long long v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    long long excl = run + incl - n;
+    unsigned hit = __ballot_sync(0xffffffffu, n > 0 && excl <= s && s < excl + n);
+    if (hit) {
+      int src = __ffs(hit) - 1;
+      if (lane == src) {
+        // Binary search the query row: largest i with tiles_before(i) <= s - excl.
+        long long off = s - excl;
+        int lo = 0, hi = r.q_len - 1;
+        while (lo < hi) {
+          int mid = (lo + hi + 1) >> 1;
+          if (req_tiles_before(r, mid) <= off) lo = mid; else hi = mid - 1;
+        }
+        cur->b = b;
+        cur->i = lo;
+        cur->t = (int)(off - req_tiles_before(r, lo));
+        cur->g = s;
+        cur->tile0 = excl;
+      }
+      int bb = __shfl_sync(0xffffffffu, cur->b, src);
+      int ii = __shfl_sync(0xffffffffu, cur->i, src);
+      int tt = __shfl_sync(0xffffffffu, cur->t, src);
+      long long t0 = __shfl_sync(0xffffffffu, cur->tile0, src);
+      cur->b = bb; cur->i = ii; cur->t = tt; cur->g = s; cur->tile0 = t0;
+      break;
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return T;
+}
+
+// One segment of a worker's range: tiles [t_begin, t_end) of one query row.
+struct Segment {
+  int row;          // global query row (decode: request)
+  int b;            // request
+  int kv0;          // first kv_indices entry of the request
+  int len;          // keys the row sees
+  int t_begin, t_end;
+  int slot;         // partial-result slot of this worker: 0 = first segment, 1 = other
+  bool whole;       // the segment covers the whole row (final output written directly)
+  bool first;       // first segment of this worker
+  long long row_tile0;  // global index of the row's first tile
+};
+
+// Sequential walk over a worker's segments (every thread of a CTA may run its own
+// copy; all copies see the same sequence).
+struct Walker {
+  PlanArgs p;
+  long long g, end;   // next global tile, end of the worker's range
+  int b, i, t;
+  long long req_tile0;
+  Req r;
+  bool started;
+
+  __device__ void init(const PlanArgs& pa, const Cursor& c, long long T, int w, int G) {
+    p = pa;
+    g = c.g;
+    end = (T == 0) ? 0 : worker_start(w + 1, T, G);
+    b = c.b; i = c.i; t = c.t; req_tile0 = c.tile0;
+    started = false;
+    if (g < end && b < p.batch) r = load_req(p, b);
+  }
+
+  __device__ bool next(Segment& s) {
+    if (g >= end) return false;
+    // Skip rows without tiles (empty requests, rows seeing no key).
+    while (true) {
+      if (i >= r.q_len) {
+        req_tile0 += req_tiles(r);
+        ++b;
+        i = 0;
+        t = 0;
+        if (b >= p.batch) return false;
+        r = load_req(p, b);
+        continue;
+      }
+      if (row_tiles(row_len(r, i)) == 0) { ++i; t = 0; continue; }
+      break;
+    }
+    const int nt = row_tiles(row_len(r, i));
+    const long long avail = end - g;
+    const int t_end = (int)min((long long)nt, (long long)t + avail);
+    s.row = r.qo0 + i;
+    s.b = b;
+    s.kv0 = r.kv0;
+    s.len = (int)row_len(r, i);
+    s.t_begin = t;
+    s.t_end = t_end;
+    s.first = !started;
+    s.slot = started ? 1 : 0;
+    s.whole = (t == 0 && t_end == nt);
+    s.row_tile0 = req_tile0 + req_tiles_before(r, i);
+    started = true;
+    g += t_end - t;
+    if (t_end == nt) { ++i; t = 0; } else { t = t_end; }
+    return true;
+  }
+};
+
+// Per-worker record read by the combine kernel: the row this worker must merge.
+struct CombineRecord {
+  int row;         // -1: nothing to merge
+  int w_first;     // first worker holding a fragment of the row
+  int slot_first;  // slot of that worker's fragment
+  int total_tiles; // T of the call (to skip workers with an empty range)
+};
+
+// Record for worker w given its first segment (or none).
+__device__ __forceinline__ CombineRecord make_record(bool has_first, const Segment& s,
+                                                     long long T, int G) {
+  CombineRecord rec{-1, 0, 0, (int)T};
+  // A row is merged by the worker holding its last tile.  If this worker's first
+  // segment ends a row that began in an earlier worker, that is this worker.
+  if (has_first && !s.whole && s.t_begin > 0 && s.t_end == row_tiles(s.len)) {
+    rec.row = s.row;
+    rec.w_first = worker_of(s.row_tile0, T, G);
+    rec.slot_first = (worker_start(rec.w_first, T, G) == s.row_tile0) ? 0 : 1;
+  }
+  return rec;
+}
+
+}  // namespace mla

@@ -1,0 +1,198 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Tolerances (max-abs): 2e-2 on the bf16 output, 1e-3 on the fp32 natural-log lse.
+Small cases compare every element; the full-size named workloads run in the
+launch configuration the benchmark times and compare sampled rows, each
+computed by the oracle one at a time.
+"""
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+from paged_head_latent_gb300 import workloads as wl
+from tests.conftest import require_gpu
+from tests.oracle_io import oracle_rows_decode, oracle_rows_prefill, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 2e-2
+LSE_TOL = 1e-3
+
+
+def run_gpu(lib, w, **kw):
+    require_gpu()
+    wd = w.to("cuda")
+    out, lse = lib.run_workload(wd, **kw)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def assert_close(out, lse, ref_out, ref_lse, what=""):
+    assert out.shape == ref_out.shape and lse.shape == ref_lse.shape
+    fin = np.isfinite(ref_lse)
+    assert np.array_equal(np.isfinite(lse), fin), f"{what}: lse finiteness differs"
+    assert np.all(np.isneginf(lse[~fin])), f"{what}: empty rows must have lse = -inf"
+    eo = np.max(np.abs(out - ref_out)) if out.size else 0.0
+    el = np.max(np.abs(lse[fin] - ref_lse[fin])) if fin.any() else 0.0
+    assert eo <= OUT_TOL, f"{what}: max |out - oracle| = {eo}"
+    assert el <= LSE_TOL, f"{what}: max |lse - oracle| = {el}"
+
+
+def check_full(lib, w, **kw):
+    out, lse = run_gpu(lib, w, **kw)
+    ref_out, ref_lse = oracle_run(w)
+    assert_close(out, lse, ref_out, ref_lse, w.name)
+    return out, lse
+
+
+# --------------------------------------------------------------- small decode
+
+def test_decode_small_named(lib):
+    check_full(lib, wl.decode_b4_h16_ps64())
+
+
+@pytest.mark.parametrize("heads", [1, 16, 64, 100, 128])
+def test_decode_head_counts(lib, heads):
+    w = wl.make_decode([1, 63, 64, 65, 127, 128, 200], num_qo_heads=heads, page_size=64, seed=2000 + heads)
+    check_full(lib, w)
+
+
+@pytest.mark.parametrize("page_size,shuffle", [(1, False), (16, False), (64, True), (32, True)])
+def test_decode_page_layouts(lib, page_size, shuffle):
+    w = wl.make_decode([3, 64, 129, 700, 31], num_qo_heads=128, page_size=page_size, seed=2100 + page_size,
+                       token_shuffle=shuffle)
+    check_full(lib, w)
+
+
+def test_decode_empty_request(lib):
+    w = wl.make_decode([0, 5, 0, 130], num_qo_heads=32, page_size=16, seed=2201)
+    check_full(lib, w)
+
+
+def test_decode_all_empty(lib):
+    w = wl.make_decode([0, 0], num_qo_heads=8, page_size=16, seed=2202)
+    check_full(lib, w)
+
+
+def test_decode_nan_in_unreferenced_slots(lib):
+    w = wl.make_decode([1, 63, 65, 200, 5], num_qo_heads=128, page_size=64, seed=2203, pool_pages=12)
+    ref_out, ref_lse = oracle_run(w)
+    out, lse = run_gpu(lib, wl.poison_unreferenced(w))
+    assert np.all(np.isfinite(out))
+    assert_close(out, lse, ref_out, ref_lse, "poisoned")
+
+
+@pytest.mark.parametrize("workers", [1, 2, 3, 7, 40, 200])
+def test_decode_split_count(lib, workers):
+    """Any number of split-KV workers gives the oracle's answer (within tolerance)."""
+    w = wl.make_decode([1000, 64, 1, 333, 2049], num_qo_heads=128, page_size=64, seed=2300)
+    check_full(lib, w, num_workers=workers)
+
+
+def test_decode_deterministic(lib):
+    w = wl.make_decode([1000, 64, 1, 333, 2049], num_qo_heads=128, page_size=64, seed=2301)
+    a = run_gpu(lib, w, num_workers=11)
+    b = run_gpu(lib, w, num_workers=11)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_decode_long_request_last(lib):
+    """Skewed batch with the long request last (the named skew workload has it first)."""
+    w = wl.make_decode([512] * 7 + [20000], num_qo_heads=128, page_size=64, seed=2302)
+    check_full(lib, w)
+
+
+# -------------------------------------------------------------- small prefill
+
+@pytest.mark.parametrize("q_lens,prefixes,heads,ps", [
+    ([5, 3], [2, 64], 2, 64),
+    ([64, 65, 1], [0, 63, 200], 16, 64),
+    ([130, 17], [70, 0], 128, 1),
+    ([100], [0], 128, 16),
+])
+def test_prefill_small(lib, q_lens, prefixes, heads, ps):
+    w = wl.make_prefill(q_lens, prefixes, num_qo_heads=heads, page_size=ps, seed=2400 + sum(q_lens))
+    check_full(lib, w)
+
+
+@pytest.mark.parametrize("workers", [1, 5, 76])
+def test_prefill_split_count(lib, workers):
+    w = wl.make_prefill([40, 90], [30, 100], num_qo_heads=64, page_size=64, seed=2500)
+    check_full(lib, w, num_workers=workers)
+
+
+# ----------------------------------------------------------- robustness / API
+
+def test_validate_flag(lib):
+    require_gpu()
+    w = wl.make_decode([5, 70], num_qo_heads=16, page_size=64, seed=2600).to("cuda")
+    ws = torch.zeros(lib.workspace_bytes(lib.make_dims(2, 16, w.num_pages, 64, w.num_kv_indices), False),
+                     dtype=torch.uint8, device="cuda")
+    lib.run_workload(w, workspace=ws, flags=lib.MLA_VALIDATE)
+    assert lib.read_device_status(ws) == 0
+    bad = w.kv_indices.clone()
+    bad[3] = w.num_pages * w.page_size + 5  # out of range: reads zeros, flagged
+    w2 = dataclasses.replace(w, kv_indices=bad)
+    lib.run_workload(w2, workspace=ws, flags=lib.MLA_VALIDATE)
+    assert lib.read_device_status(ws) == -6
+    assert lib.read_device_status(ws) == 0  # the word was cleared
+
+
+def test_cuda_graph_capture(lib):
+    require_gpu()
+    w = wl.make_decode([100, 2000, 7], num_qo_heads=128, page_size=64, seed=2700).to("cuda")
+    out = torch.empty(3, 128, 512, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(3, 128, dtype=torch.float32, device="cuda")
+    ws = torch.zeros(lib.workspace_bytes(lib.make_dims(3, 128, w.num_pages, 64, w.num_kv_indices), False),
+                     dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        lib.run_workload(w, out=out, lse=lse, workspace=ws, stream=s)  # warm-up (tensor maps cached)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    ref = (out.clone(), lse.clone())
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        lib.run_workload(w, out=out, lse=lse, workspace=ws, stream=torch.cuda.current_stream())
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref[0]) and torch.equal(lse, ref[1])
+
+
+# ------------------------------------------------------- full-size workloads
+
+def _sample_rows(n, extra=()):
+    rng = np.random.default_rng(7)
+    picks = set(int(x) for x in rng.choice(n, size=min(n, 6), replace=False))
+    picks.update(int(x) % n for x in extra)
+    return sorted(picks)
+
+
+@pytest.mark.parametrize("name", ["decode_b64_h128_ps64", "decode_b128_h128_ps1", "decode_b32_h128_skew"])
+def test_full_size_decode_sampled(lib, name):
+    w = wl.by_name(name)
+    out, lse = run_gpu(lib, w)
+    lens = w.kv_lens()
+    rows = _sample_rows(w.batch, extra=(0, w.batch - 1, int(np.argmax(lens)), int(np.argmin(lens))))
+    ref = oracle_rows_decode(w, rows)
+    for r in rows:
+        assert_close(out[r], lse[r], ref[r][0], ref[r][1], f"{name} row {r}")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
+
+
+def test_full_size_prefill_sampled(lib):
+    w = wl.prefill_causal_h128()
+    out, lse = run_gpu(lib, w)
+    qo = w.qo_indptr.tolist()
+    extra = [qo[b] for b in range(4)] + [qo[b + 1] - 1 for b in range(4)] + [qo[b] + 63 for b in range(4)] \
+        + [qo[b] + 64 for b in range(4)]
+    rows = _sample_rows(w.rows, extra=extra)
+    ref = oracle_rows_prefill(w, rows)
+    for r in rows:
+        assert_close(out[r], lse[r], ref[r][0], ref[r][1], f"prefill row {r}")
+    assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
