@@ -6,9 +6,10 @@
 
 namespace mla {
 
-// The attention kernel over all workers: writes whole rows to out/lse and split
-// rows' fragments to the workspace, plus each worker's combine record.
-cudaError_t launch_attention(const MlaParams& p, cudaStream_t stream);
+// CUDA-core attention kernel (16 heads per CTA), same partition and outputs as the
+// tensor-core kernel: whole rows to out/lse, split rows' fragments to the workspace,
+// and each worker's combine record.
+cudaError_t launch_simt(const MlaParams& p, cudaStream_t stream);
 // Merge of split rows' fragments (one CTA per worker and head).
 cudaError_t launch_combine(const MlaParams& p, cudaStream_t stream);
 // Optional index validation (sets the status word; never traps).

@@ -3,17 +3,22 @@
 // Every entry point only enqueues work on the caller's stream; nothing here
 // synchronises or reads device memory except mla_read_device_status and
 // mla_profile_read, which exist to do exactly that.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <vector>
 
 #include "../../include/mla_paged.h"
 #include "common.cuh"
 #include "launch.h"
+#include "tc_kernel.h"
 
 namespace {
 
@@ -77,6 +82,91 @@ int resolve_workers(const mla_dims* d, int* G) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---------------------------------------------------------------- TMA descriptors
+using EncodeFn = PFN_cuTensorMapEncodeTiled_v12000;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(f);
+    cudaGetLastError();
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void* ptr;
+  uint64_t rows, cols;
+  uint32_t box_rows;
+  int promo;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && promo == o.promo;
+  }
+};
+
+struct MapCache {
+  std::mutex mu;
+  std::vector<std::pair<MapKey, CUtensorMap>> entries;  // most recent last
+} g_maps;
+
+// 2-D bf16 map over [rows, cols] (row stride = cols), box = 64 columns x box_rows, 128-byte swizzle.
+int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+            CUtensorMapL2promotion promo) {
+  if (rows == 0) {  // nothing can be loaded: the kernel is given no keys / rows for it
+    std::memset(out, 0, sizeof(*out));
+    return MLA_OK;
+  }
+  const MapKey key{ptr, rows, cols, box_rows, (int)promo};
+  std::lock_guard<std::mutex> lk(g_maps.mu);
+  for (auto& e : g_maps.entries)
+    if (e.first == key) {
+      *out = e.second;
+      return MLA_OK;
+    }
+  EncodeFn fn = encode_fn();
+  if (!fn) return MLA_ERR_CUDA;
+  alignas(64) CUtensorMap m;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
+  if (g_maps.entries.size() >= 96) g_maps.entries.erase(g_maps.entries.begin());
+  g_maps.entries.emplace_back(key, m);
+  *out = m;
+  return MLA_OK;
+}
+
+int build_maps(const MlaParams& p, mla::TmaMaps* m) {
+  const uint64_t qrows = (uint64_t)p.rows * p.heads;
+  const uint64_t slots = (uint64_t)p.num_slots;
+  int st;
+  if ((st = get_map(&m->q_nope, p.q_nope, qrows, 512, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
+  if ((st = get_map(&m->q_pe, p.q_pe, qrows, 64, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
+  if ((st = get_map(&m->ckv, p.ckv, slots, 512, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
+  if ((st = get_map(&m->kpe, p.kpe, slots, 64, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
+  if ((st = get_map(&m->ckv_g, p.ckv, slots, 512, 1, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
+  if ((st = get_map(&m->kpe_g, p.kpe, slots, 64, 1, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
+  return MLA_OK;
+}
+
+bool force_simt() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("MLA_FORCE_SIMT");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 // ---------------------------------------------------------------- profiling
 struct ProfileState {
   bool on = false;
@@ -105,7 +195,9 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   int st = check_dims(dims, prefill);
   if (st != MLA_OK) return st;
   const long long rows = prefill ? dims->total_q : dims->batch;
-  if (!q_nope || !q_pe || !ckv_cache || !kpe_cache || !kv_indptr || !out || !lse) return MLA_ERR_NULL;
+  if (!q_nope || !q_pe || !kv_indptr || !out || !lse) return MLA_ERR_NULL;
+  // The caches may be NULL only when they hold no slot at all.
+  if ((!ckv_cache || !kpe_cache) && dims->num_pages > 0) return MLA_ERR_NULL;
   if (prefill && !qo_indptr) return MLA_ERR_NULL;
   if (dims->num_kv_indices > 0 && !kv_indices) return MLA_ERR_NULL;
   if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
@@ -138,7 +230,8 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   p.heads = dims->num_qo_heads;
   p.rows = (int)rows;
   p.num_slots = dims->num_pages * dims->page_size;
-  p.num_kv_indices = dims->num_kv_indices;
+  // With an empty cache no key can be loaded: treat every request as empty.
+  p.num_kv_indices = p.num_slots > 0 ? dims->num_kv_indices : 0;
   p.workers = G;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
@@ -154,7 +247,14 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   }
   cudaEvent_t* ev = profile_slot();
   if (ev) cudaEventRecord(ev[0], stream);
-  if (mla::launch_attention(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  if (force_simt()) {
+    if (mla::launch_simt(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  } else {
+    mla::TmaMaps maps;
+    st = build_maps(p, &maps);
+    if (st != MLA_OK) return st;
+    if (mla::launch_tc(maps, p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+  }
   if (ev) cudaEventRecord(ev[1], stream);
   if (mla::launch_combine(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
   if (ev) cudaEventRecord(ev[2], stream);

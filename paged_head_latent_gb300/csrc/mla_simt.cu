@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kSimtThreads) mla_simt_kernel(MlaParams prm) {
   if (blockIdx.y == 0 && tid == 0) prm.records[w] = make_record(have_first, first_seg, T, prm.workers);
 }
 
-cudaError_t launch_attention(const MlaParams& p, cudaStream_t stream) {
+cudaError_t launch_simt(const MlaParams& p, cudaStream_t stream) {
   static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
