@@ -256,7 +256,7 @@ def our_arm(args, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
         # keep sampling long enough for a few readings when the timed loop was short
-        while time.perf_counter() - wall0 < 1.0:
+        while not args.quick and time.perf_counter() - wall0 < 1.0:
             with torch.cuda.stream(stream):
                 for _ in range(20):
                     call()
@@ -279,11 +279,11 @@ def our_arm(args, rank, world, local_rank):
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    e2e_steps = max(3, min(args.steps, 30))
+    e2e_steps = 0 if args.quick else max(3, min(args.steps, 30))
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        for it in range(e2e_steps + 2):
+        for it in range(e2e_steps + 2 if e2e_steps else 0):
             if it == 2:
                 e0.record(stream)
             for k, t in host.items():
@@ -291,9 +291,10 @@ def our_arm(args, rank, world, local_rank):
             call()
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(lse, non_blocking=True)
-        e1.record(stream)
+        if e2e_steps:
+            e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan")
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -311,7 +312,7 @@ def our_arm(args, rank, world, local_rank):
     ach_tflops = flops / (main_avg_ms * 1e-3) / 1e12
     roof_time_us = max(nbytes / (hbm * 1e9), flops / (tc * 1e12)) * 1e6
     cpu = None
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not args.quick:
         secs, ck, cr = time_oracle(w_cpu, args.cpu_seconds)
         cpu_us = secs / max(ck, 1) * keys * 1e6
         cpu = {"value": cpu_us, "unit": "us/call", "cores": cores_used(), "kind": "oracle",
@@ -351,6 +352,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quick", action="store_true",
+                    help="profiling runs: no clock soak, no end-to-end leg, no CPU baseline")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -103,10 +103,11 @@ EncodeFn encode_fn() {
 struct MapKey {
   const void* ptr;
   uint64_t rows, cols;
-  uint32_t box_rows;
-  int promo;
+  uint32_t box_cols, box_rows;
+  int swizzle, promo;
   bool operator==(const MapKey& o) const {
-    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_rows == o.box_rows && promo == o.promo;
+    return ptr == o.ptr && rows == o.rows && cols == o.cols && box_cols == o.box_cols && box_rows == o.box_rows &&
+           swizzle == o.swizzle && promo == o.promo;
   }
 };
 
@@ -115,14 +116,14 @@ struct MapCache {
   std::vector<std::pair<MapKey, CUtensorMap>> entries;  // most recent last
 } g_maps;
 
-// 2-D bf16 map over [rows, cols] (row stride = cols), box = 64 columns x box_rows, 128-byte swizzle.
-int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
-            CUtensorMapL2promotion promo) {
+// 2-D bf16 map over [rows, cols] (row stride = cols), box = box_cols x box_rows.
+int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
+            CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
   if (rows == 0) {  // nothing can be loaded: the kernel is given no keys / rows for it
     std::memset(out, 0, sizeof(*out));
     return MLA_OK;
   }
-  const MapKey key{ptr, rows, cols, box_rows, (int)promo};
+  const MapKey key{ptr, rows, cols, box_cols, box_rows, (int)swizzle, (int)promo};
   std::lock_guard<std::mutex> lk(g_maps.mu);
   for (auto& e : g_maps.entries)
     if (e.first == key) {
@@ -134,10 +135,10 @@ int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uin
   alignas(64) CUtensorMap m;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
   if (g_maps.entries.size() >= 96) g_maps.entries.erase(g_maps.entries.begin());
   g_maps.entries.emplace_back(key, m);
@@ -145,16 +146,21 @@ int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uin
   return MLA_OK;
 }
 
+// The attention kernel's tensor maps: 64-column ckv boxes in 128-byte swizzle (one
+// 64-slot page, or one gathered row), 32-column kpe boxes in 64-byte swizzle (each CTA
+// of a pair takes half of the 64 positional dims), and query rows (L2 prefetch only).
 int build_maps(const MlaParams& p, mla::TmaMaps* m) {
   const uint64_t qrows = (uint64_t)p.rows * p.heads;
   const uint64_t slots = (uint64_t)p.num_slots;
+  const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+  const auto l256 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B, l128 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   int st;
-  if ((st = get_map(&m->q_nope, p.q_nope, qrows, 512, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
-  if ((st = get_map(&m->q_pe, p.q_pe, qrows, 64, 128, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
-  if ((st = get_map(&m->ckv, p.ckv, slots, 512, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
-  if ((st = get_map(&m->kpe, p.kpe, slots, 64, 64, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
-  if ((st = get_map(&m->ckv_g, p.ckv, slots, 512, 1, CU_TENSOR_MAP_L2_PROMOTION_L2_256B)) != MLA_OK) return st;
-  if ((st = get_map(&m->kpe_g, p.kpe, slots, 64, 1, CU_TENSOR_MAP_L2_PROMOTION_L2_128B)) != MLA_OK) return st;
+  if ((st = get_map(&m->q_nope, p.q_nope, qrows, 512, 64, 128, sw128, l256)) != MLA_OK) return st;
+  if ((st = get_map(&m->q_pe, p.q_pe, qrows, 64, 64, 128, sw128, l128)) != MLA_OK) return st;
+  if ((st = get_map(&m->ckv, p.ckv, slots, 512, 64, 64, sw128, l256)) != MLA_OK) return st;
+  if ((st = get_map(&m->kpe, p.kpe, slots, 64, 32, 64, sw64, l128)) != MLA_OK) return st;
+  if ((st = get_map(&m->ckv_g, p.ckv, slots, 512, 64, 1, sw128, l256)) != MLA_OK) return st;
+  if ((st = get_map(&m->kpe_g, p.kpe, slots, 64, 32, 1, sw64, l128)) != MLA_OK) return st;
   return MLA_OK;
 }
 

@@ -10,48 +10,73 @@
 
 namespace mla {
 
-constexpr int kCombineThreads = 128;  // 128 threads x 4 dims = 512
+constexpr int kCombineWarps = 8;  // one warp per head, 8 heads per CTA
+constexpr int kCombineThreads = 32 * kCombineWarps;
+
+// Fragment f (0-based, worker w_first + f) of a record: its slot index in the workspace,
+// or -1 if that worker has an empty range (possible only when tiles < workers).
+__device__ __forceinline__ long long frag_index(const CombineRecord& rec, int f, int G) {
+  const int wk = rec.w_first + f;
+  const long long T = rec.total_tiles;
+  if (worker_start(wk + 1, T, G) == worker_start(wk, T, G)) return -1;
+  return (long long)wk * 2 + (f == 0 ? rec.slot_first : 0);
+}
 
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams p) {
   const int w = blockIdx.x;
-  const int h = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kCombineWarps + warp;
   const CombineRecord rec = p.records[w];
   if (rec.row < 0 || h >= p.heads) return;
-  const long long T = rec.total_tiles;
   const int G = p.workers;
+  const int F = w - rec.w_first + 1;
+  // Pass 1: lse of every fragment (lanes in parallel), max and sum by warp shuffles.
   float mx = -INFINITY;
-  for (int f = rec.w_first; f <= w; ++f) {
-    if (worker_start(f + 1, T, G) == worker_start(f, T, G)) continue;  // empty range
-    const int slot = (f == rec.w_first) ? rec.slot_first : 0;
-    mx = fmaxf(mx, p.part_lse[((size_t)f * 2 + slot) * p.heads + h]);
+  for (int f = lane; f < F; f += 32) {
+    const long long fi = frag_index(rec, f, G);
+    if (fi >= 0) mx = fmaxf(mx, p.part_lse[fi * p.heads + h]);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
-  for (int f = rec.w_first; f <= w; ++f) {
-    if (worker_start(f + 1, T, G) == worker_start(f, T, G)) continue;
-    const int slot = (f == rec.w_first) ? rec.slot_first : 0;
-    sum += fast_exp2(p.part_lse[((size_t)f * 2 + slot) * p.heads + h] - mx);
+  for (int f = lane; f < F; f += 32) {
+    const long long fi = frag_index(rec, f, G);
+    if (fi >= 0) sum += fast_exp2(p.part_lse[fi * p.heads + h] - mx);
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
   const float lse2 = mx + fast_log2(sum);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int f = rec.w_first; f <= w; ++f) {
-    if (worker_start(f + 1, T, G) == worker_start(f, T, G)) continue;
-    const int slot = (f == rec.w_first) ? rec.slot_first : 0;
-    const size_t frag = ((size_t)f * 2 + slot) * p.heads + h;
+  // Pass 2: out = sum_f 2^(lse_f - lse) o_f, in fragment order; lane owns dims
+  // 4*lane + 128*q (q = 0..3) so each load instruction of the warp is one 512-byte row.
+  float4 acc[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int f = 0; f < F; ++f) {
+    const long long fi = frag_index(rec, f, G);
+    if (fi < 0) continue;
+    const size_t frag = (size_t)fi * p.heads + h;
     const float wgt = fast_exp2(p.part_lse[frag] - lse2);
-    const float4 v = reinterpret_cast<const float4*>(p.part_o + frag * kDimCkv)[threadIdx.x];
-    acc.x = fmaf(wgt, v.x, acc.x);
-    acc.y = fmaf(wgt, v.y, acc.y);
-    acc.z = fmaf(wgt, v.z, acc.z);
-    acc.w = fmaf(wgt, v.w, acc.w);
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + frag * kDimCkv);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float4 v = src[lane + 32 * q];
+      acc[q].x = fmaf(wgt, v.x, acc[q].x);
+      acc[q].y = fmaf(wgt, v.y, acc[q].y);
+      acc[q].z = fmaf(wgt, v.z, acc[q].z);
+      acc[q].w = fmaf(wgt, v.w, acc[q].w);
+    }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-  uint2 packed;
-  packed.x = *reinterpret_cast<uint32_t*>(&lo);
-  packed.y = *reinterpret_cast<uint32_t*>(&hi);
   __nv_bfloat16* dst = p.out + ((size_t)rec.row * p.heads + h) * kDimCkv;
-  reinterpret_cast<uint2*>(dst)[threadIdx.x] = packed;
-  if (threadIdx.x == 0) p.lse[(size_t)rec.row * p.heads + h] = lse2 * 0.69314718055994531f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[q].x, acc[q].y);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[q].z, acc[q].w);
+    uint2 packed;
+    packed.x = *reinterpret_cast<uint32_t*>(&lo);
+    packed.y = *reinterpret_cast<uint32_t*>(&hi);
+    reinterpret_cast<uint2*>(dst)[lane + 32 * q] = packed;
+  }
+  if (lane == 0) p.lse[(size_t)rec.row * p.heads + h] = lse2 * 0.69314718055994531f;
 }
 
 // Index validation (flashinfer's "validate" switch on its planned wrapper inspired it):
@@ -88,7 +113,7 @@ __global__ void mla_validate_kernel(MlaParams p) {
 }
 
 cudaError_t launch_combine(const MlaParams& p, cudaStream_t stream) {
-  mla_combine_kernel<<<dim3(p.workers, p.heads), kCombineThreads, 0, stream>>>(p);
+  mla_combine_kernel<<<dim3(p.workers, (p.heads + kCombineWarps - 1) / kCombineWarps), kCombineThreads, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

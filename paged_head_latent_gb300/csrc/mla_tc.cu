@@ -11,25 +11,38 @@
 //
 // How the pair splits the work.  O for 128 heads x 512 fp32 needs all 512 TMEM
 // columns of an SM, which would leave none for S.  So CTA rank r owns
-// O[:, 256r : 256r+256] (256 columns) and loads only the key columns it needs:
-//   rank 0: ckv[:, 0:256]                 (scores over dims 0..255, V for dims 0..255)
-//   rank 1: ckv[:, 256:512] and kpe[:, :]  (scores over dims 256..575, V for dims 256..511)
+// O[:, 256r : 256r+256] and a 288-wide slice of the 576-wide query-key depth:
+//   rank r: ckv[:, 256r : 256r+256] (its V columns too) and kpe[:, 32r : 32r+32].
 // Each CTA computes a partial S over its depth slice; the two partial S tiles are
 // swapped through distributed shared memory (st.async) and added, so every score is
 // computed once and both CTAs see identical S (fp32 addition commutes), hence take
 // identical softmax decisions.  This is the left/right split of the output that
 // FlashMLA's "seesaw" schedule uses across two warpgroups (oL, oR), done here across
-// the two SMs of a cluster with the query-key depth split as well.
+// the two SMs of a cluster with the depth split as well.
 //
-// Warp roles (192 threads per CTA):
-//   warps 0-3  softmax / correction / epilogue: thread = TMEM lane = query head
-//   warp 4     TMA producer: Q tiles, and 64-key ckv/kpe tiles -- one box load per
-//              column chunk when the tile's 64 slots are contiguous (a whole page of
-//              64), else tile::gather4 row loads; rows past the row's length read a
-//              slot index outside the cache, which TMA fills with zeros
-//   warp 5     MMA issuer (one thread) and TMEM owner
-// Shared memory: Q (<= 5 x 16 KB), 2 KV stages (<= 5 x 8 KB each), P (16 KB bf16),
-// the partial-S exchange buffer (32 KB), mbarriers.
+// Tensor memory (496 of 512 columns): O half (256 fp32), S (64 fp32), P (32 columns
+// of packed bf16 pairs) and this CTA's Q slice (144 columns of bf16 pairs), so both
+// products read one operand from TMEM: S = Q.K^T and O += P.V are TS-form tcgen05.mma.
+// Shared memory: a 4-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
+// 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 32 KB)
+// and two small reduction buffers.
+//
+// Warp roles (320 threads per CTA):
+//   warps 0-7  softmax / correction / epilogue / Q loading.  Warp w serves TMEM lanes
+//              32*(w%4) .. +31 (lane = query head) and key columns 32*(w/4) .. +31 of
+//              each tile; the two warps of a lane group combine their row maxima through
+//              shared memory and a 64-thread named barrier.  The loop is software
+//              pipelined: tile j+1's partial S leaves for the peer before tile j's
+//              softmax runs.
+//   warp 8     TMA producer: one box load per column chunk when the tile's 64 slots
+//              are contiguous (a whole page of 64), else tile::gather4 row loads; rows
+//              past the row's length read a slot outside the cache, which TMA fills
+//              with zeros.  It also warms L2 with the tiles and query rows it will
+//              need next (cp.async.bulk.prefetch.tensor).
+//   warp 9     MMA issuer (one thread), issuing QK two tiles ahead of PV, and TMEM owner.
+// The exchange needs no "buffer free" signal: the peer refills buffer b with tile
+// j+2 only after it has received this CTA's tile j+1, which each thread sends after
+// it has read tile j from buffer b.
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -41,79 +54,141 @@ using namespace ptx;
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kProducerWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr int kStages = 2;
-constexpr uint32_t kChunkQ = 128 * 128;  // 128 rows x 64 bf16
-constexpr uint32_t kChunkKV = 64 * 128;  // 64 rows x 64 bf16
-constexpr uint32_t kStageBytes = 5 * kChunkKV;
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffKV = kOffQ + 5 * kChunkQ;
-constexpr uint32_t kOffP = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffX = kOffP + 128 * 128;
-constexpr uint32_t kOffBar = kOffX + 128 * 64 * 4;
-constexpr uint32_t kSmemBytes = kOffBar + 256 + 1024;  // + alignment slack
+constexpr int kSoftmaxWarps = 8;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr int kPrefetchTiles = 8;           // L2 look-ahead of the producer, in tiles
+constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
+constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
+constexpr uint32_t kChunkPe = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
+constexpr uint32_t kStageBytes = 4 * kChunkKV + kChunkPe;
+constexpr uint32_t kXBytes = 128 * 64 * 4;  // one partial-S tile, fp32
+constexpr uint32_t kOffKV = 0;
+constexpr uint32_t kOffX = kOffKV + kStages * kStageBytes;
+constexpr uint32_t kOffRed = kOffX + 2 * kXBytes;  // [2][2][128] row maxima
+constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;  // [2][128] row sums
+constexpr uint32_t kOffDesc = kOffL + 2 * 128 * 4;  // ring of kDescRing tile descriptors
+constexpr int kDescRing = 8;
+constexpr uint32_t kOffBar = kOffDesc + kDescRing * 32;
+constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColO = 0;
-constexpr uint32_t kColS = 256;  // two 64-column S buffers
-constexpr uint32_t kXBytes = 128 * 64 * 4;
-constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by > 2^8
+constexpr uint32_t kColO = 0;    // 256 columns
+constexpr uint32_t kColS = 256;  // 64 columns
+constexpr uint32_t kColP = 320;  // 32 columns
+constexpr uint32_t kColQ = 352;  // 144 columns
+constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by more than 2^8
 
 enum Bar : uint32_t {
-  Q_FULL, Q_EMPTY, KV_FULL0, KV_FULL1, KV_EMPTY0, KV_EMPTY1, S_FULL0, S_FULL1, S_EMPTY0, S_EMPTY1,
-  P_FULL, PV_DONE, X_FULL, X_FREE, O_FULL, O_EMPTY, DRAIN, NUM_BARS
+  Q_FULL, KV_FULL0, KV_EMPTY0 = KV_FULL0 + kStages, S_FULL = KV_EMPTY0 + kStages, S_EMPTY, P_FULL, PV_DONE,
+  X_FULL0, X_FULL1, O_FULL, O_EMPTY, DRAIN, NUM_BARS
 };
 
-static_assert(kOffBar + NUM_BARS * 8 <= kOffBar + 256, "barrier area");
+struct Misc {
+  uint32_t tmem;
+  int abort;
+  long long T;
+  Cursor cur;
+};
+
+static_assert(NUM_BARS * 8 <= 256, "barrier area");
+static_assert(sizeof(Misc) <= 64, "misc area");
 static_assert(kSmemBytes <= 232448, "shared memory");
+static_assert(kStageBytes % 1024 == 0, "stage alignment");
+
+__device__ __forceinline__ void pair_sync(int warp) {
+  // The two softmax warps that serve the same TMEM lanes (w and w + 4).
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+}
+
+// Tiles of a worker in order, with their segment.
+struct TileIter {
+  Walker walk;
+  Segment seg;
+  int t;
+  int nseg;  // index of seg among the worker's segments
+  bool live;
+  __device__ void init(const PlanArgs& pa, const Cursor& c, long long T, int w, int G) {
+    walk.init(pa, c, T, w, G);
+    nseg = -1;
+    live = walk.next(seg);
+    if (live) {
+      t = seg.t_begin;
+      nseg = 0;
+    }
+  }
+  __device__ bool first() const { return t == seg.t_begin; }
+  __device__ bool last() const { return t == seg.t_end - 1; }
+  __device__ void advance() {
+    if (++t == seg.t_end) {
+      live = walk.next(seg);
+      if (live) {
+        t = seg.t_begin;
+        ++nseg;
+      }
+    }
+  }
+};
+
+// What the MMA and softmax roles need to know about one tile; written by the
+// producer into a ring of kDescRing entries (slot j % kDescRing) before it issues the
+// tile's loads, and read after the tile's KV_FULL barrier has completed.  A slot is
+// rewritten only for tile j + kDescRing, i.e. after P.V of tile j + kDescRing - kStages,
+// by which time every reader of tile j is done with it.
+struct TileDesc {
+  int t;         // tile within the query row
+  int len;       // keys the row sees
+  int row;       // query row (decode: request)
+  int slot;      // partial-result slot of the segment
+  int nseg;      // index of the segment among this worker's segments
+  int flags;     // kFirst | kLast | kWhole
+  int next_row;  // query row of the next segment when kLast, else -1
+  int pad;
+};
+constexpr int kFirst = 1, kLast = 2, kWhole = 4;
+static_assert(sizeof(TileDesc) == 32, "descriptor size");
 
 }  // namespace
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ uint32_t sh_tmem;
-  __shared__ int sh_abort;
-  __shared__ Cursor sh_cur;
-  __shared__ long long sh_T;
-
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
+  Misc& misc = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int w = blockIdx.x >> 1;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int nchunks = rank ? 5 : 4;  // Q and KV column chunks of this CTA
-  volatile int* abort = &sh_abort;
+  volatile int* abort = &misc.abort;
   auto bar = [&](uint32_t i) { return sbase + kOffBar + 8u * i; };
 
   if (threadIdx.x == 0) {
-    sh_abort = 0;
-    mbar_init(bar(Q_FULL), 1);
-    mbar_init(bar(Q_EMPTY), 1);
+    misc.abort = (sbase & 1023u) ? 1 : 0;  // swizzled tiles need 1 KB alignment
+    if (misc.abort) atomicOr(p.status, kStatusTimeout);
+    mbar_init(bar(Q_FULL), kSoftmaxWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(KV_FULL0 + s), 1);
       mbar_init(bar(KV_EMPTY0 + s), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(S_FULL0 + b), 1);
-      mbar_init(bar(S_EMPTY0 + b), 4);
-    }
-    mbar_init(bar(P_FULL), 4);
+    mbar_init(bar(S_FULL), 1);
+    mbar_init(bar(S_EMPTY), kSoftmaxWarps);
+    mbar_init(bar(P_FULL), kSoftmaxWarps);
     mbar_init(bar(PV_DONE), 1);
-    mbar_init(bar(X_FULL), 1);
-    mbar_init(bar(X_FREE), 4);
+    mbar_init(bar(X_FULL0), 1);
+    mbar_init(bar(X_FULL1), 1);
     mbar_init(bar(O_FULL), 1);
-    mbar_init(bar(O_EMPTY), 4);
+    mbar_init(bar(O_EMPTY), kSoftmaxWarps);
     mbar_init(bar(DRAIN), 1);
     fence_mbar_init();
-    // Arm the first phase of the exchange barrier before the peer can send.
-    mbar_arrive_expect_tx(bar(X_FULL), kXBytes);
+    // Arm the first phase of both exchange barriers before the peer can send.
+    mbar_arrive_expect_tx(bar(X_FULL0), kXBytes);
+    mbar_arrive_expect_tx(bar(X_FULL1), kXBytes);
   }
   if (warp == kMmaWarp) {
-    tmem_alloc(smem_u32(&sh_tmem), kTmemCols);
+    tmem_alloc(sbase + kOffMisc, kTmemCols);  // misc.tmem is the first word of Misc
     tmem_relinquish();
   }
   const PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices};
@@ -121,8 +196,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     Cursor c;
     const long long T = warp_plan(pa, w, p.workers, &c);
     if (lane == 0) {
-      sh_cur = c;
-      sh_T = T;
+      misc.cur = c;
+      misc.T = T;
     }
     if (w == 0 && rank == 0) warp_write_empty_rows(p);
   }
@@ -130,156 +205,191 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   __syncthreads();
   cluster_sync();
   tc_fence_after();
-  const uint32_t tmem = sh_tmem;
-  const long long T = sh_T;
+  const uint32_t tmem = misc.tmem;
+  const long long T = misc.abort ? 0 : misc.T;
+  const Cursor cur = misc.cur;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      prefetch_tensormap(&maps.q_nope);
-      prefetch_tensormap(&maps.q_pe);
       prefetch_tensormap(&maps.ckv);
       prefetch_tensormap(&maps.kpe);
       prefetch_tensormap(&maps.ckv_g);
       prefetch_tensormap(&maps.kpe_g);
     }
-    Walker walk;
-    walk.init(pa, sh_cur, T, w, p.workers);
-    Segment seg;
+    // Slot ids of tile t of a segment: lanes hold keys lane and lane + 32; keys past
+    // the row's length get a slot outside the cache (TMA reads zeros there).
+    auto tile_slots = [&](const Segment& sg, int t, int& s0, int& s1, bool& contiguous, int& first) {
+      const int key0 = t * kTileKeys;
+      const int nvalid = min(kTileKeys, sg.len - key0);
+      const int* ip = p.kv_indices + sg.kv0 + key0;
+      s0 = lane < nvalid ? __ldg(ip + lane) : p.num_slots;
+      s1 = lane + 32 < nvalid ? __ldg(ip + lane + 32) : p.num_slots;
+      first = __shfl_sync(0xffffffffu, s0, 0);
+      const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
+                       first <= p.num_slots - kTileKeys;
+      contiguous = __all_sync(0xffffffffu, run);
+    };
+    // Rows 4g .. 4g+3 of the tile for lane g < 16.
+    auto gather_rows = [&](int s0, int s1, int (&r)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int key = 4 * (lane & 15) + q;
+        const int v0 = __shfl_sync(0xffffffffu, s0, key & 31);
+        const int v1 = __shfl_sync(0xffffffffu, s1, key & 31);
+        r[q] = key < 32 ? v0 : v1;
+      }
+    };
+    const int ckv_col = (int)rank * 256;
+    const int kpe_col = (int)rank * 32;
+    // Look-ahead: warm L2 with what the ring will need kPrefetchTiles tiles from now.
+    TileIter ahead;
+    ahead.init(pa, cur, T, w, p.workers);
+    auto prefetch_next = [&]() {
+      if (!ahead.live) return;
+      if (ahead.first() && lane == 0) {
+        const int qrow = ahead.seg.row * p.heads;
+        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&maps.q_nope, ckv_col + c * 64, qrow);
+        tma_prefetch_2d(&maps.q_pe, 0, qrow);
+      }
+      int s0, s1, first;
+      bool contiguous;
+      tile_slots(ahead.seg, ahead.t, s0, s1, contiguous, first);
+      if (contiguous) {
+        if (lane == 0) {
+          for (int c = 0; c < 4; ++c) tma_prefetch_2d(&maps.ckv, ckv_col + c * 64, first);
+          tma_prefetch_2d(&maps.kpe, kpe_col, first);
+        }
+      } else {
+        int r[4];
+        gather_rows(s0, s1, r);
+        if (lane < 16) {
+          for (int c = 0; c < 4; ++c) tma_prefetch_gather4(&maps.ckv_g, ckv_col + c * 64, r[0], r[1], r[2], r[3]);
+          tma_prefetch_gather4(&maps.kpe_g, kpe_col, r[0], r[1], r[2], r[3]);
+        }
+      }
+      ahead.advance();
+    };
+    for (int i = 0; i < kPrefetchTiles; ++i) prefetch_next();
+
+    TileIter it;
+    it.init(pa, cur, T, w, p.workers);
+    if (rank == 0 && lane == 0) p.records[w] = make_record(it.live, it.seg, T, p.workers);
+    TileDesc* desc = reinterpret_cast<TileDesc*>(smem + kOffDesc);
     uint32_t j = 0;
-    int nseg = 0;
-    int q_issued = 0;
-    bool ok = true;
-    while (ok && walk.next(seg)) {
-      if (nseg > 0 && !mbar_wait(bar(Q_EMPTY), (nseg - 1) & 1, abort, p.status, kStatusTimeout)) break;
-      ++q_issued;
+    for (; it.live; it.advance(), ++j) {
+      const int stage = j % kStages;
+      int s0, s1, first;
+      bool contiguous;
+      // Slot ids first, so their load overlaps the wait for a free stage.
+      tile_slots(it.seg, it.t, s0, s1, contiguous, first);
+      prefetch_next();
+      if (j >= kStages &&
+          !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout))
+        break;
+      const uint32_t kvbar = bar(KV_FULL0 + stage);
+      const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
       if (lane == 0) {
-        mbar_arrive_expect_tx(bar(Q_FULL), nchunks * kChunkQ);
-        const int qrow = seg.row * p.heads;
-        for (int c = 0; c < 4; ++c)
-          tma_load_2d(sbase + kOffQ + c * kChunkQ, &maps.q_nope, (int)rank * 256 + c * 64, qrow, bar(Q_FULL));
-        if (rank) tma_load_2d(sbase + kOffQ + 4 * kChunkQ, &maps.q_pe, 0, qrow, bar(Q_FULL));
+        TileDesc d;
+        d.t = it.t;
+        d.len = it.seg.len;
+        d.row = it.seg.row;
+        d.slot = it.seg.slot;
+        d.nseg = it.nseg;
+        d.flags = (it.first() ? kFirst : 0) | (it.last() ? kLast : 0) | (it.seg.whole ? kWhole : 0);
+        d.next_row = -1;
+        if (it.last()) {
+          TileIter peek = it;
+          peek.advance();
+          if (peek.live) d.next_row = peek.seg.row;
+        }
+        desc[j % kDescRing] = d;
+        mbar_arrive_expect_tx(kvbar, kStageBytes);  // release: orders the descriptor before the tile
       }
       __syncwarp();
-      for (int t = seg.t_begin; t < seg.t_end; ++t, ++j) {
-        const int stage = j % kStages;
-        const int key0 = t * kTileKeys;
-        const int nvalid = min(kTileKeys, seg.len - key0);
-        // Slot ids of the tile (read before waiting so the load overlaps the wait).
-        const int* ip = p.kv_indices + seg.kv0 + key0;
-        const int s0 = lane < nvalid ? __ldg(ip + lane) : p.num_slots;
-        const int s1 = lane + 32 < nvalid ? __ldg(ip + lane + 32) : p.num_slots;
-        if (j >= kStages &&
-            !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout)) {
-          ok = false;
-          break;
+      if (contiguous) {
+        if (lane == 0) {
+          for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kChunkKV, &maps.ckv, ckv_col + c * 64, first, kvbar);
+          tma_load_2d(dst + 4 * kChunkKV, &maps.kpe, kpe_col, first, kvbar);
         }
-        const int first = __shfl_sync(0xffffffffu, s0, 0);
-        const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
-                         first <= p.num_slots - kTileKeys;
-        const bool contiguous = __all_sync(0xffffffffu, run);
-        const uint32_t kvbar = bar(KV_FULL0 + stage);
-        const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
-        if (lane == 0) mbar_arrive_expect_tx(kvbar, nchunks * kChunkKV);
-        __syncwarp();
-        if (contiguous) {
-          if (lane == 0) {
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(dst + c * kChunkKV, &maps.ckv, (int)rank * 256 + c * 64, first, kvbar);
-            if (rank) tma_load_2d(dst + 4 * kChunkKV, &maps.kpe, 0, first, kvbar);
-          }
-        } else {
-          // Lane g < 16 gathers rows 4g .. 4g+3 of the tile.
-          int r[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int key = 4 * (lane & 15) + q;
-            const int v0 = __shfl_sync(0xffffffffu, s0, key & 31);
-            const int v1 = __shfl_sync(0xffffffffu, s1, key & 31);
-            r[q] = key < 32 ? v0 : v1;
-          }
-          if (lane < 16) {
-            for (int c = 0; c < 4; ++c)
-              tma_gather4(dst + c * kChunkKV + lane * 512, &maps.ckv_g, (int)rank * 256 + c * 64, r[0], r[1], r[2],
-                          r[3], kvbar);
-            if (rank) tma_gather4(dst + 4 * kChunkKV + lane * 512, &maps.kpe_g, 0, r[0], r[1], r[2], r[3], kvbar);
-          }
+      } else {
+        int r[4];
+        gather_rows(s0, s1, r);
+        if (lane < 16) {
+          for (int c = 0; c < 4; ++c)
+            tma_gather4(dst + c * kChunkKV + lane * 512, &maps.ckv_g, ckv_col + c * 64, r[0], r[1], r[2], r[3],
+                        kvbar);
+          tma_gather4(dst + 4 * kChunkKV + lane * 256, &maps.kpe_g, kpe_col, r[0], r[1], r[2], r[3], kvbar);
         }
-        __syncwarp();
       }
-      ++nseg;
+      __syncwarp();
     }
-    // Drain: wait (bounded) for the last loads into every stage and for Q, so no copy
-    // is in flight when the CTA exits, whatever happened above.
+    // Drain: wait (bounded) for the last load into every stage, so no copy is in
+    // flight when the CTA exits, whatever happened above.
     if (lane == 0) {
       volatile int no_abort = 0;
       for (uint32_t s = 0; s < kStages && s < j; ++s) {
-        const uint32_t last = j - 1 - ((j - 1 - s) % kStages);  // last tile issued into stage (last % kStages)
+        const uint32_t last = j - 1 - ((j - 1 - s) % kStages);
         mbar_wait(bar(KV_FULL0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout);
       }
-      if (q_issued > 0) mbar_wait(bar(Q_FULL), (q_issued - 1) & 1, &no_abort, p.status, kStatusTimeout);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
-      Walker walk;
-      walk.init(pa, sh_cur, T, w, p.workers);
-      Segment seg;
-      uint32_t j = 0;
-      int nseg = 0;
+      const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
+      const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
+      uint32_t jq = 0, jv = 0;  // next tile to score (QK), next tile to accumulate (PV)
       bool ok = true;
-      // O += P . V for global tile jj (the P of that tile is in smem).
-      auto pv = [&](uint32_t jj, bool first_of_seg, int segno) -> bool {
-        if (!mbar_wait(bar(P_FULL), jj & 1, abort, p.status, kStatusTimeout)) return false;
-        if (first_of_seg && segno > 0 &&
-            !mbar_wait(bar(O_EMPTY), (segno - 1) & 1, abort, p.status, kStatusTimeout))
+      // S = Q . K^T for tile jq (TS form: Q slice in TMEM, K tile in shared memory).
+      auto qk = [&]() -> bool {
+        const uint32_t stage = jq % kStages;
+        if (!mbar_wait(bar(KV_FULL0 + stage), (jq / kStages) & 1, abort, p.status, kStatusTimeout)) return false;
+        const TileDesc d = desc[jq % kDescRing];
+        if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout)) ||
+            (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout)))
           return false;
         tc_fence_after();
-        const uint32_t stage = jj % kStages;
+        const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < kQkSteps; ++kk) {
+          const uint64_t b = kk < 16 ? smem_desc_sw128(kv + (kk >> 2) * kChunkKV + (kk & 3) * 32, 16, 1024)
+                                     : smem_desc_sw64(kv + 4 * kChunkKV + (kk - 16) * 32, 16, 512);
+          mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * kk, b, kIdescQK, kk != 0 ? 1u : 0u);
+        }
+        mma_commit(bar(S_FULL));
+        ++jq;
+        return true;
+      };
+      // O += P . V for tile jv (TS form: P in TMEM, V = the ckv half of the tile).
+      auto pv = [&]() -> bool {
+        const uint32_t stage = jv % kStages;
+        const TileDesc d = desc[jv % kDescRing];
+        const bool first = d.flags & kFirst;
+        if (!mbar_wait(bar(P_FULL), jv & 1, abort, p.status, kStatusTimeout) ||
+            (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout)))
+          return false;
+        tc_fence_after();
         const uint32_t vbase = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint64_t a = smem_desc_sw128(sbase + kOffP + k * 32, 16, 1024);
           const uint64_t b = smem_desc_sw128(vbase + k * 2048, kChunkKV, 1024);
-          mma_bf16_ss(tmem + kColO, a, b, kIdescPV, (first_of_seg && k == 0) ? 0u : 1u);
+          mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, b, kIdescPV, (first && k == 0) ? 0u : 1u);
         }
         mma_commit(bar(KV_EMPTY0 + stage));
         mma_commit(bar(PV_DONE));
+        if (d.flags & kLast) mma_commit(bar(O_FULL));
+        ++jv;
         return true;
       };
-      while (ok && walk.next(seg)) {
-        if (!mbar_wait(bar(Q_FULL), nseg & 1, abort, p.status, kStatusTimeout)) break;
-        for (int t = seg.t_begin; t < seg.t_end; ++t, ++j) {
-          const uint32_t stage = j % kStages;
-          const uint32_t buf = j & 1;
-          if (!mbar_wait(bar(KV_FULL0 + stage), (j / kStages) & 1, abort, p.status, kStatusTimeout) ||
-              (j >= 2 && !mbar_wait(bar(S_EMPTY0 + buf), ((j >> 1) - 1) & 1, abort, p.status, kStatusTimeout))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kvbase = sbase + kOffKV + stage * kStageBytes;
-          for (int c = 0; c < nchunks; ++c) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t a = smem_desc_sw128(sbase + kOffQ + c * kChunkQ + k * 32, 16, 1024);
-              const uint64_t b = smem_desc_sw128(kvbase + c * kChunkKV + k * 32, 16, 1024);
-              mma_bf16_ss(tmem + kColS + 64 * buf, a, b, kIdescQK, (c | k) != 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(bar(S_FULL0 + buf));
-          if (t == seg.t_end - 1) mma_commit(bar(Q_EMPTY));
-          if (t > seg.t_begin && !pv(j - 1, t - 1 == seg.t_begin, nseg)) {
-            ok = false;
-            break;
-          }
-        }
-        if (!ok) break;
-        if (!pv(j - 1, seg.t_end - 1 == seg.t_begin, nseg)) break;
-        mma_commit(bar(O_FULL));
-        ++nseg;
+      // QK runs ahead of PV: the softmax warps read tile j+1's scores at the start of
+      // iteration j, so QK(j+1) must be issued before the MMA thread blocks on P(j-1).
+      // Order: QK0 QK1 QK2 PV0 QK3 PV1 QK4 PV2 ...
+      while (ok && jq < ntiles && jq < 3) ok = qk();
+      while (ok && jv < ntiles) {
+        ok = pv();
+        if (ok && jq < ntiles) ok = qk();
       }
       // Drain: every MMA issued above has completed once DRAIN fires.
       mma_commit(bar(DRAIN));
@@ -289,180 +399,228 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int row = threadIdx.x;  // TMEM lane == query head
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int row = threadIdx.x & 127;  // TMEM lane == query head
+    const int half = warp >> 2;         // key columns 32*half .. +31 of each tile
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t x_local = sbase + kOffX;
     const uint32_t x_remote = mapa(x_local, peer);
-    const uint32_t xfull_remote = mapa(bar(X_FULL), peer);
-    const uint32_t xfree_remote = mapa(bar(X_FREE), peer);
-    const uint32_t p_row = sbase + kOffP + (row >> 3) * 1024 + (row & 7) * 128;
+    const uint32_t xfull_remote0 = mapa(bar(X_FULL0), peer);
+    const uint32_t xfull_remote1 = mapa(bar(X_FULL1), peer);
+    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    float* lbuf = reinterpret_cast<float*>(smem + kOffL);
     const float scale = p.scale_log2;
-    Walker walk;
-    walk.init(pa, sh_cur, T, w, p.workers);
-    Segment seg, first_seg{};
-    bool have_first = false;
-    uint32_t j = 0;
-    int nseg = 0;
-    bool ok = true;
-    while (ok && walk.next(seg)) {
-      if (seg.first) {
-        have_first = true;
-        first_seg = seg;
-      }
-      float m_ref = -INFINITY, l = 0.f;
-      for (int t = seg.t_begin; t < seg.t_end; ++t, ++j) {
-        const int nvalid = min(kTileKeys, seg.len - t * kTileKeys);
-        const uint32_t buf = j & 1;
-        if (!mbar_wait(bar(S_FULL0 + buf), (j >> 1) & 1, abort, p.status, kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sa[32], sb[32];
-        tmem_ld32(tmem + lane_base + kColS + 64 * buf, sa);
-        tmem_ld32(tmem + lane_base + kColS + 64 * buf + 32, sb);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(S_EMPTY0 + buf));
-        // Swap partial scores with the peer CTA.
-        if (j > 0 && !mbar_wait<true>(bar(X_FREE), (j - 1) & 1, abort, p.status, kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_remote + (c * 128 + row) * 16, sa[4 * c], sa[4 * c + 1], sa[4 * c + 2], sa[4 * c + 3],
-                      xfull_remote);
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          st_async_v4(x_remote + ((c + 8) * 128 + row) * 16, sb[4 * c], sb[4 * c + 1], sb[4 * c + 2],
-                      sb[4 * c + 3], xfull_remote);
-        if (!mbar_wait<true>(bar(X_FULL), j & 1, abort, p.status, kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-        float s[64];
-        const float4* xin = reinterpret_cast<const float4*>(smem + kOffX);
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          const float4 v = xin[c * 128 + row];
-          const uint32_t* mine = c < 8 ? &sa[4 * c] : &sb[4 * (c - 8)];
-          s[4 * c + 0] = __uint_as_float(mine[0]) + v.x;
-          s[4 * c + 1] = __uint_as_float(mine[1]) + v.y;
-          s[4 * c + 2] = __uint_as_float(mine[2]) + v.z;
-          s[4 * c + 3] = __uint_as_float(mine[3]) + v.w;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(xfree_remote);
-        if (threadIdx.x == 0) mbar_arrive_expect_tx(bar(X_FULL), kXBytes);  // arm the next phase
-        // Online softmax in base 2.
-        float mx = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 64; ++k) {
-          s[k] = k < nvalid ? s[k] * scale : -INFINITY;
-          mx = fmaxf(mx, s[k]);
-        }
-        float alpha = 1.f;
-        bool rescale = false;
-        if (t == seg.t_begin) {
-          m_ref = mx;
-        } else if (mx > m_ref + kRescaleLog2) {
-          alpha = fast_exp2(m_ref - mx);
-          m_ref = mx;
-          l *= alpha;
-          rescale = true;
-        }
-        uint32_t pk[32];
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float a = fast_exp2(s[2 * k] - m_ref);
-          const float b = fast_exp2(s[2 * k + 1] - m_ref);
-          sum += a + b;
-          __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
-          pk[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        l += sum;
-        // The previous tile's P . V must be done before P is overwritten and O rescaled.
-        if (j > 0 && !mbar_wait(bar(PV_DONE), (j - 1) & 1, abort, p.status, kStatusTimeout)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-          for (int cc = 0; cc < 8; ++cc) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st32(tmem + lane_base + kColO + cc * 32, o);
-          }
-          tmem_st_wait();
-        }
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t addr = p_row + ((c ^ (row & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * c]), "r"(pk[4 * c + 1]),
-                       "r"(pk[4 * c + 2]), "r"(pk[4 * c + 3])
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(P_FULL));
-      }
-      if (!ok) break;
-      // Epilogue: O / l to out (whole rows) or to the workspace (split rows).
-      if (!mbar_wait(bar(O_FULL), nseg & 1, abort, p.status, kStatusTimeout)) break;
-      tc_fence_after();
-      const float inv_l = 1.f / l;
-      const float lse2 = m_ref + fast_log2(l);
+
+    // Write the Q slice of query row `qrow` (this thread's head, this half's columns)
+    // into TMEM: half 0 -> depth 0..127 (16 x 16 B of q_nope), half 1 -> depth
+    // 128..287 (16 x 16 B of q_nope, 4 x 16 B of q_pe).  Heads >= H get zeros.
+    auto write_q = [&](int qrow) {
       const bool valid = row < p.heads;
-      const size_t frag = ((size_t)w * 2 + seg.slot) * p.heads + row;
-#pragma unroll 1
-      for (int cc = 0; cc < 8; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + cc * 32, o);
-        tmem_ld_wait();
-        const int d0 = (int)rank * 256 + cc * 32;
-        if (valid) {
-          if (seg.whole) {
-            uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)seg.row * p.heads + row) * kDimCkv + d0);
+      const size_t rg = (size_t)qrow * p.heads + row;
+      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + rg * kDimCkv + rank * 256 + half * 128);
+      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + rg * kDimKpe + rank * 32);
+      const uint32_t col = tmem + lane_base + kColQ + half * 64;
+      const int nvec = half ? 20 : 16;  // 16-byte pieces of this thread's slice
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t wds[4];
+      for (int r0 = 0; r0 < 20; r0 += 8) {
+        if (r0 >= nvec) break;
+        uint4 v[8];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
-                                                         __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
-                wds[e] = *reinterpret_cast<uint32_t*>(&h);
-              }
-              dst[q] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + frag * kDimCkv + d0);
+        for (int i = 0; i < 8; ++i) {
+          const int k = r0 + i;
+          v[i] = make_uint4(0, 0, 0, 0);
+          if (valid && k < nvec) v[i] = k < 16 ? __ldg(qn + k) : __ldg(qp + (k - 16));
+        }
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                   __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+        for (int c = 0; c < 2; ++c) {
+          if (r0 + 4 * c >= nvec) break;
+          uint32_t rr[16];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            rr[4 * i + 0] = v[4 * c + i].x;
+            rr[4 * i + 1] = v[4 * c + i].y;
+            rr[4 * i + 2] = v[4 * c + i].z;
+            rr[4 * i + 3] = v[4 * c + i].w;
           }
+          tmem_st16(col + 4 * (r0 + 4 * c), rr);  // 16 bytes = 4 columns of bf16 pairs
         }
       }
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(O_EMPTY));
-      if (valid && rank == 0) {
-        if (seg.whole)
-          p.lse[(size_t)seg.row * p.heads + row] = lse2 * 0.69314718055994531f;
-        else
-          p.part_lse[frag] = lse2;
+      if (lane == 0) mbar_arrive(bar(Q_FULL));
+    };
+
+    const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
+    const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
+    bool ok = true;
+    uint32_t jf = 0;  // tiles fetched
+    uint32_t sn[32];  // partial scores of the last fetched tile
+    // Fetch tile jf, part 1: read its partial S from TMEM, release S, and write the
+    // next segment's Q slice if this was the segment's last QK.
+    auto fetch_scores = [&]() -> bool {
+      if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout)) return false;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(S_EMPTY));
+      // The tile's descriptor: its KV_FULL phase has completed (QK read the tile).
+      if (!mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout))
+        return false;
+      const int next_row = desc[jf % kDescRing].next_row;
+      if (next_row >= 0) write_q(next_row);
+      return true;
+    };
+    // Part 2: send the partial to the peer (exchange buffer jf & 1).
+    auto send_scores = [&]() {
+      const uint32_t b = jf & 1;
+      const uint32_t xoff = b * kXBytes;
+      const uint32_t xr = b ? xfull_remote1 : xfull_remote0;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        st_async_v4(x_remote + xoff + ((8 * half + c) * 128 + row) * 16, sn[4 * c], sn[4 * c + 1], sn[4 * c + 2],
+                    sn[4 * c + 3], xr);
+      ++jf;
+    };
+
+    if (ntiles > 0) {
+      if (!mbar_wait(bar(KV_FULL0), 0, abort, p.status, kStatusTimeout)) {
+        ok = false;
+      } else {
+        write_q(desc[0].row);
+        ok = fetch_scores();
+        if (ok) send_scores();
       }
-      ++nseg;
     }
-    if (rank == 0 && threadIdx.x == 0) p.records[w] = make_record(have_first, first_seg, T, p.workers);
+    float m_ref = -INFINITY, l = 0.f;  // l: this thread's 32 columns only
+    uint32_t j = 0;
+    while (ok && j < jf) {
+      const TileDesc cd = desc[j % kDescRing];  // tile j (KV_FULL seen in fetch_scores)
+      const uint32_t b = j & 1;
+      if (!mbar_wait<true>(bar(X_FULL0 + b), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
+      float s[32];
+      const float4* xin = reinterpret_cast<const float4*>(smem + kOffX + b * kXBytes);
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        const float4 v = xin[(8 * half + c) * 128 + row];
+        s[4 * c + 0] = __uint_as_float(sn[4 * c + 0]) + v.x;
+        s[4 * c + 1] = __uint_as_float(sn[4 * c + 1]) + v.y;
+        s[4 * c + 2] = __uint_as_float(sn[4 * c + 2]) + v.z;
+        s[4 * c + 3] = __uint_as_float(sn[4 * c + 3]) + v.w;
+      }
+      if (threadIdx.x == 0) mbar_arrive_expect_tx(bar(X_FULL0 + b), kXBytes);  // arm its next use
+      // Tile j+1's scores leave for the peer only after buffer b has been read (see
+      // the header), and before tile j's softmax runs.
+      if (jf < ntiles) {
+        if (!fetch_scores()) break;
+        send_scores();
+      }
+      const int nvalid = min(kTileKeys, cd.len - cd.t * kTileKeys) - 32 * half;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        s[k] = k < nvalid ? s[k] * scale : -INFINITY;
+        mx = fmaxf(mx, s[k]);
+      }
+      red[(b * 2 + half) * 128 + row] = mx;
+      pair_sync(warp);
+      mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
+      float alpha = 1.f;
+      bool rescale = false;
+      if (cd.flags & kFirst) {
+        m_ref = mx;
+        l = 0.f;
+      } else if (mx > m_ref + kRescaleLog2) {
+        alpha = fast_exp2(m_ref - mx);
+        m_ref = mx;
+        l *= alpha;
+        rescale = true;
+      }
+      uint32_t pk[16];
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float a = fast_exp2(s[2 * k] - m_ref);
+        const float bb = fast_exp2(s[2 * k + 1] - m_ref);
+        sum += a + bb;
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
+        pk[k] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      l += sum;
+      // P is single-buffered: the previous tile's P.V must be done (it also settles O).
+      if (j >= 1 && !mbar_wait(bar(PV_DONE), (j - 1) & 1, abort, p.status, kStatusTimeout)) break;
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          const uint32_t col = tmem + lane_base + kColO + 128 * half + 32 * cc;
+          tmem_ld32(col, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+          tmem_st32(col, o);
+        }
+      }
+      tmem_st16(tmem + lane_base + kColP + 16 * half, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(P_FULL));
+
+      if (cd.flags & kLast) {
+        // Epilogue: O / l to out (whole rows) or to the workspace (split rows).
+        lbuf[half * 128 + row] = l;
+        pair_sync(warp);
+        const float lt = l + lbuf[(half ^ 1) * 128 + row];
+        if (!mbar_wait(bar(O_FULL), cd.nseg & 1, abort, p.status, kStatusTimeout)) break;
+        tc_fence_after();
+        const float inv_l = 1.f / lt;
+        const float lse2 = m_ref + fast_log2(lt);
+        const bool valid = row < p.heads;
+        const size_t frag = ((size_t)w * 2 + cd.slot) * p.heads + row;
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_base + kColO + 128 * half + 32 * cc, o);
+          tmem_ld_wait();
+          const int d0 = (int)rank * 256 + 128 * half + cc * 32;
+          if (valid) {
+            if (cd.flags & kWhole) {
+              uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)cd.row * p.heads + row) * kDimCkv + d0);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t wds[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
+                                                           __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
+                  wds[e] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                dst[q] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+              }
+            } else {
+              float4* dst = reinterpret_cast<float4*>(p.part_o + frag * kDimCkv + d0);
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
+                                     __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(O_EMPTY));
+        if (valid && rank == 0 && half == 0) {
+          if (cd.flags & kWhole)
+            p.lse[(size_t)cd.row * p.heads + row] = lse2 * 0.69314718055994531f;
+          else
+            p.part_lse[frag] = lse2;
+        }
+      }
+      ++j;
+    }
   }
 
   tc_fence_before();

@@ -7,14 +7,14 @@
 
 namespace mla {
 
-// 2-D bf16 tensor maps, 128-byte swizzle, 64-column boxes.
+// 2-D bf16 tensor maps (box = columns x rows).
 struct TmaMaps {
-  CUtensorMap q_nope;  // [rows*H, 512], box 64 x 128 (all heads of one query row)
-  CUtensorMap q_pe;    // [rows*H, 64],  box 64 x 128
-  CUtensorMap ckv;     // [slots, 512],  box 64 x 64 (a whole 64-slot page)
-  CUtensorMap kpe;     // [slots, 64],   box 64 x 64
-  CUtensorMap ckv_g;   // [slots, 512],  box 64 x 1 (tile::gather4 rows)
-  CUtensorMap kpe_g;   // [slots, 64],   box 64 x 1
+  CUtensorMap q_nope;  // [rows*H, 512], box 64 x 128, 128-byte swizzle (L2 prefetch of query rows)
+  CUtensorMap q_pe;    // [rows*H, 64],  box 64 x 128, 128-byte swizzle (L2 prefetch)
+  CUtensorMap ckv;     // [slots, 512],  box 64 x 64, 128-byte swizzle (a whole 64-slot page)
+  CUtensorMap kpe;     // [slots, 64],   box 32 x 64, 64-byte swizzle (half of the positional dims)
+  CUtensorMap ckv_g;   // [slots, 512],  box 64 x 1, 128-byte swizzle (tile::gather4 rows)
+  CUtensorMap kpe_g;   // [slots, 64],   box 32 x 1, 64-byte swizzle
 };
 
 cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream);

@@ -25,8 +25,11 @@ LSE_TOL = 1e-3
 def run_gpu(lib, w, **kw):
     require_gpu()
     wd = w.to("cuda")
-    out, lse = lib.run_workload(wd, **kw)
-    torch.cuda.synchronize()
+    dims = lib.make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
+                         total_q=w.rows if w.kind == "prefill" else 0, num_workers=kw.get("num_workers", 0))
+    ws = torch.zeros(lib.workspace_bytes(dims, w.kind == "prefill"), dtype=torch.uint8, device="cuda")
+    out, lse = lib.run_workload(wd, workspace=ws, **kw)
+    assert lib.read_device_status(ws) == 0, "device status word reports an error (bounded wait gave up?)"
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
