@@ -15,7 +15,7 @@
 #include <mutex>
 #include <vector>
 
-#include "../../include/mla_paged.h"
+#include "mla_paged.h"
 #include "common.cuh"
 #include "launch.h"
 #include "tc_kernel.h"

@@ -23,11 +23,12 @@
 // Tensor memory (496 of 512 columns): O half (256 fp32), S (64 fp32), P (32 columns
 // of packed bf16 pairs) and this CTA's Q slice (144 columns of bf16 pairs), so both
 // products read one operand from TMEM: S = Q.K^T and O += P.V are TS-form tcgen05.mma.
-// Shared memory: a 4-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
+// Shared memory: a 3-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
 // 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 32 KB)
-// and two small reduction buffers.
+// that the peer fills, one 32 KB staging buffer for the outgoing partial (sent with a
+// shared::cta -> shared::cluster bulk copy), and small reduction buffers.
 //
-// Warp roles (320 threads per CTA):
+// Warp roles (352 threads per CTA):
 //   warps 0-7  softmax / correction / epilogue / Q loading.  Warp w serves TMEM lanes
 //              32*(w%4) .. +31 (lane = query head) and key columns 32*(w/4) .. +31 of
 //              each tile; the two warps of a lane group combine their row maxima through
@@ -37,9 +38,10 @@
 //   warp 8     TMA producer: one box load per column chunk when the tile's 64 slots
 //              are contiguous (a whole page of 64), else tile::gather4 row loads; rows
 //              past the row's length read a slot outside the cache, which TMA fills
-//              with zeros.  It also warms L2 with the tiles and query rows it will
-//              need next (cp.async.bulk.prefetch.tensor).
-//   warp 9     MMA issuer (one thread), issuing QK two tiles ahead of PV, and TMEM owner.
+//              with zeros.
+//   warp 9     issues S = Q.K^T (one thread) and owns TMEM
+//   warp 10    issues O += P.V (one thread); tcgen05.mma issue blocks while the tensor
+//              pipe is busy, so the two products get separate issuing threads.
 // The exchange needs no "buffer free" signal: the peer refills buffer b with tile
 // j+2 only after it has received this CTA's tile j+1, which each thread sends after
 // it has read tile j from buffer b.
@@ -56,10 +58,10 @@ namespace {
 
 constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
-constexpr int kStages = 4;
-constexpr int kPrefetchTiles = 8;           // L2 look-ahead of the producer, in tiles
+constexpr int kMmaWarp = 9;    // issues S = Q.K^T; owns TMEM
+constexpr int kPvWarp = 10;    // issues O += P.V
+constexpr int kThreads = 352;
+constexpr int kStages = 3;
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kChunkPe = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
@@ -67,7 +69,8 @@ constexpr uint32_t kStageBytes = 4 * kChunkKV + kChunkPe;
 constexpr uint32_t kXBytes = 128 * 64 * 4;  // one partial-S tile, fp32
 constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffX = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffRed = kOffX + 2 * kXBytes;  // [2][2][128] row maxima
+constexpr uint32_t kOffOut = kOffX + 2 * kXBytes;  // outgoing partial S (staging for the bulk copy)
+constexpr uint32_t kOffRed = kOffOut + kXBytes;    // [2][2][128] row maxima
 constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;  // [2][128] row sums
 constexpr uint32_t kOffDesc = kOffL + 2 * 128 * 4;  // ring of kDescRing tile descriptors
 constexpr int kDescRing = 8;
@@ -97,6 +100,9 @@ static_assert(NUM_BARS * 8 <= 256, "barrier area");
 static_assert(sizeof(Misc) <= 64, "misc area");
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
+
+// All eight softmax warps.
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 5, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void pair_sync(int warp) {
   // The two softmax warps that serve the same TMEM lanes (w and w + 4).
@@ -181,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(X_FULL1), 1);
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), kSoftmaxWarps);
-    mbar_init(bar(DRAIN), 1);
+    mbar_init(bar(DRAIN), 2);  // one commit from each MMA-issuing thread
     fence_mbar_init();
     // Arm the first phase of both exchange barriers before the peer can send.
     mbar_arrive_expect_tx(bar(X_FULL0), kXBytes);
@@ -242,36 +248,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
     const int ckv_col = (int)rank * 256;
     const int kpe_col = (int)rank * 32;
-    // Look-ahead: warm L2 with what the ring will need kPrefetchTiles tiles from now.
-    TileIter ahead;
-    ahead.init(pa, cur, T, w, p.workers);
-    auto prefetch_next = [&]() {
-      if (!ahead.live) return;
-      if (ahead.first() && lane == 0) {
-        const int qrow = ahead.seg.row * p.heads;
-        for (int c = 0; c < 4; ++c) tma_prefetch_2d(&maps.q_nope, ckv_col + c * 64, qrow);
-        tma_prefetch_2d(&maps.q_pe, 0, qrow);
-      }
-      int s0, s1, first;
-      bool contiguous;
-      tile_slots(ahead.seg, ahead.t, s0, s1, contiguous, first);
-      if (contiguous) {
-        if (lane == 0) {
-          for (int c = 0; c < 4; ++c) tma_prefetch_2d(&maps.ckv, ckv_col + c * 64, first);
-          tma_prefetch_2d(&maps.kpe, kpe_col, first);
-        }
-      } else {
-        int r[4];
-        gather_rows(s0, s1, r);
-        if (lane < 16) {
-          for (int c = 0; c < 4; ++c) tma_prefetch_gather4(&maps.ckv_g, ckv_col + c * 64, r[0], r[1], r[2], r[3]);
-          tma_prefetch_gather4(&maps.kpe_g, kpe_col, r[0], r[1], r[2], r[3]);
-        }
-      }
-      ahead.advance();
-    };
-    for (int i = 0; i < kPrefetchTiles; ++i) prefetch_next();
-
     TileIter it;
     it.init(pa, cur, T, w, p.workers);
     if (rank == 0 && lane == 0) p.records[w] = make_record(it.live, it.seg, T, p.workers);
@@ -283,7 +259,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool contiguous;
       // Slot ids first, so their load overlaps the wait for a free stage.
       tile_slots(it.seg, it.t, s0, s1, contiguous, first);
-      prefetch_next();
       if (j >= kStages &&
           !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout))
         break;
@@ -333,65 +308,60 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(bar(KV_FULL0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kPvWarp) {
+    // ------------------------------------------------------------ MMA issuers
+    // tcgen05.mma issue blocks while the tensor pipe is busy, so QK and PV come from
+    // two threads: PV(j) goes out as soon as P(j) exists instead of queueing behind the
+    // issue of a later QK, which frees the tile's stage for the producer sooner.
     if (lane == 0) {
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
       const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
       const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
-      uint32_t jq = 0, jv = 0;  // next tile to score (QK), next tile to accumulate (PV)
-      bool ok = true;
-      // S = Q . K^T for tile jq (TS form: Q slice in TMEM, K tile in shared memory).
-      auto qk = [&]() -> bool {
-        const uint32_t stage = jq % kStages;
-        if (!mbar_wait(bar(KV_FULL0 + stage), (jq / kStages) & 1, abort, p.status, kStatusTimeout)) return false;
-        const TileDesc d = desc[jq % kDescRing];
-        if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout)) ||
-            (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout)))
-          return false;
-        tc_fence_after();
-        const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
+      if (warp == kMmaWarp) {
+        // S = Q . K^T for every tile (TS form: Q slice in TMEM, K tile in shared memory).
+        for (uint32_t jq = 0; jq < ntiles; ++jq) {
+          const uint32_t stage = jq % kStages;
+          if (!mbar_wait(bar(KV_FULL0 + stage), (jq / kStages) & 1, abort, p.status, kStatusTimeout)) break;
+          const TileDesc d = desc[jq % kDescRing];
+          if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout)) ||
+              (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout)))
+            break;
+          tc_fence_after();
+          const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < kQkSteps; ++kk) {
-          const uint64_t b = kk < 16 ? smem_desc_sw128(kv + (kk >> 2) * kChunkKV + (kk & 3) * 32, 16, 1024)
-                                     : smem_desc_sw64(kv + 4 * kChunkKV + (kk - 16) * 32, 16, 512);
-          mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * kk, b, kIdescQK, kk != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kQkSteps; ++kk) {
+            const uint64_t b = kk < 16 ? smem_desc_sw128(kv + (kk >> 2) * kChunkKV + (kk & 3) * 32, 16, 1024)
+                                       : smem_desc_sw64(kv + 4 * kChunkKV + (kk - 16) * 32, 16, 512);
+            mma_bf16_ts(tmem + kColS, tmem + kColQ + 8 * kk, b, kIdescQK, kk != 0 ? 1u : 0u);
+          }
+          mma_commit(bar(S_FULL));
         }
-        mma_commit(bar(S_FULL));
-        ++jq;
-        return true;
-      };
-      // O += P . V for tile jv (TS form: P in TMEM, V = the ckv half of the tile).
-      auto pv = [&]() -> bool {
-        const uint32_t stage = jv % kStages;
-        const TileDesc d = desc[jv % kDescRing];
-        const bool first = d.flags & kFirst;
-        if (!mbar_wait(bar(P_FULL), jv & 1, abort, p.status, kStatusTimeout) ||
-            (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout)))
-          return false;
-        tc_fence_after();
-        const uint32_t vbase = sbase + kOffKV + stage * kStageBytes;
+      } else {
+        // O += P . V for every tile (TS form: P in TMEM, V = the ckv half of the tile).
+        // The tile's descriptor is visible here: the softmax warps read it after the
+        // tile's KV_FULL and only then arrive on P_FULL.
+        for (uint32_t jv = 0; jv < ntiles; ++jv) {
+          const uint32_t stage = jv % kStages;
+          if (!mbar_wait(bar(P_FULL), jv & 1, abort, p.status, kStatusTimeout)) break;
+          const TileDesc d = desc[jv % kDescRing];
+          const bool first = d.flags & kFirst;
+          if (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout))
+            break;
+          tc_fence_after();
+          const uint32_t vbase = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint64_t b = smem_desc_sw128(vbase + k * 2048, kChunkKV, 1024);
-          mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, b, kIdescPV, (first && k == 0) ? 0u : 1u);
+          for (int k = 0; k < 4; ++k) {
+            const uint64_t b = smem_desc_sw128(vbase + k * 2048, kChunkKV, 1024);
+            mma_bf16_ts(tmem + kColO, tmem + kColP + 8 * k, b, kIdescPV, (first && k == 0) ? 0u : 1u);
+          }
+          mma_commit(bar(KV_EMPTY0 + stage));
+          mma_commit(bar(PV_DONE));
+          if (d.flags & kLast) mma_commit(bar(O_FULL));
         }
-        mma_commit(bar(KV_EMPTY0 + stage));
-        mma_commit(bar(PV_DONE));
-        if (d.flags & kLast) mma_commit(bar(O_FULL));
-        ++jv;
-        return true;
-      };
-      // QK runs ahead of PV: the softmax warps read tile j+1's scores at the start of
-      // iteration j, so QK(j+1) must be issued before the MMA thread blocks on P(j-1).
-      // Order: QK0 QK1 QK2 PV0 QK3 PV1 QK4 PV2 ...
-      while (ok && jq < ntiles && jq < 3) ok = qk();
-      while (ok && jv < ntiles) {
-        ok = pv();
-        if (ok && jq < ntiles) ok = qk();
       }
-      // Drain: every MMA issued above has completed once DRAIN fires.
+      // Drain: every MMA this thread issued has completed once DRAIN fires (it counts
+      // one commit from each of the two issuing threads).
       mma_commit(bar(DRAIN));
       volatile int no_abort = 0;
       mbar_wait(bar(DRAIN), 0, &no_abort, p.status, kStatusTimeout);
@@ -472,15 +442,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (next_row >= 0) write_q(next_row);
       return true;
     };
-    // Part 2: send the partial to the peer (exchange buffer jf & 1).
+    // Part 2: send the partial to the peer's exchange buffer jf & 1.  The threads stage
+    // it in their own shared memory (16-byte chunk c of row r at (c * 128 + r) * 16, the
+    // peer's layout) and one thread hands the 32 KB to the bulk-copy engine, so the
+    // transfer runs in the background of the softmax.  The staging buffer is rewritten
+    // only after the previous bulk copy has read it (wait_group.read before the first
+    // barrier).
+    const uint32_t out_local = sbase + kOffOut;
     auto send_scores = [&]() {
       const uint32_t b = jf & 1;
-      const uint32_t xoff = b * kXBytes;
-      const uint32_t xr = b ? xfull_remote1 : xfull_remote0;
+      if (threadIdx.x == 0) bulk_wait_group_read0();
+      softmax_sync();
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_async_v4(x_remote + xoff + ((8 * half + c) * 128 + row) * 16, sn[4 * c], sn[4 * c + 1], sn[4 * c + 2],
-                    sn[4 * c + 3], xr);
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t a = out_local + ((8 * half + c) * 128 + row) * 16;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(sn[4 * c]), "r"(sn[4 * c + 1]),
+                     "r"(sn[4 * c + 2]), "r"(sn[4 * c + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      softmax_sync();
+      if (threadIdx.x == 0) {
+        bulk_copy_to_peer(x_remote + b * kXBytes, out_local, kXBytes, b ? xfull_remote1 : xfull_remote0);
+        bulk_commit_group();
+      }
       ++jf;
     };
 
@@ -623,6 +608,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (threadIdx.x == 0) bulk_wait_group_read0();  // no bulk copy may still read our smem
   tc_fence_before();
   __syncthreads();
   cluster_sync();
