@@ -112,6 +112,28 @@ int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cach
                       const mla_dims* dims, void* workspace, size_t workspace_bytes, int flags,
                       void* stream);
 
+/*
+ * Paged MLA decode for callers that cannot allocate device memory (a plugin that runs
+ * inside another framework's memory pool, code that must not call cudaMalloc after
+ * start-up, or a context where an allocation would synchronise the device).  This entry
+ * point has no counterpart in the pages the library follows; it computes exactly what
+ * mla_paged_decode computes, with the same arguments except the workspace.
+ *
+ * The split-KV scratch lives in one static device array of 32 MiB inside the library,
+ * held by every GPU that loads the library until the process exits.  With
+ * dims->num_workers == 0 the call uses one worker per SM pair, or fewer if their
+ * partial results would not fit in the 32 MiB; an explicit num_workers whose scratch
+ * needs more returns MLA_ERR_WORKSPACE.  flags must be 0 (the device status word is not
+ * readable through this entry point), else MLA_ERR_DIMS.  All calls share the array and
+ * it keeps the last call's contents: calls that overlap on the GPU race.  The first
+ * call on each device looks up the array's address (with that device current); make it
+ * before any stream capture.  The call itself allocates nothing.
+ */
+int mla_paged_decode_noalloc(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                             const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                             float sm_scale, void* out, float* lse, const mla_dims* dims, int flags,
+                             void* stream);
+
 /* Workspace bytes a call with these dims needs (0 on invalid dims).  With
  * dims->num_workers == 0 it queries the current device's SM count. */
 size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill);

@@ -49,6 +49,8 @@ _SIGNATURES = [
     ("mla_paged_prefill", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
       ctypes.c_int, _P]),
+    ("mla_paged_decode_noalloc", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P]),
     ("mla_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
     ("mla_default_num_workers", ctypes.c_int, []),
     ("mla_status_string", ctypes.c_char_p, [ctypes.c_int]),
@@ -190,6 +192,34 @@ def mla_paged_prefill(q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, 
     """Paged MLA causal prefill, bottom-right aligned ("MLA Paged", section "prefill")."""
     return _call(True, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
                  out, lse, workspace, flags, num_workers, stream)
+
+
+def mla_paged_decode_noalloc(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale,
+                             out, lse, num_workers=0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA decode without a workspace argument, for callers that cannot allocate
+    device memory: the library's own static 32 MiB device scratch holds the split-KV
+    partials.  ``out`` and ``lse`` must be given (nothing is allocated here either).
+    Calls that overlap on the GPU race on the shared scratch."""
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache), ("kpe_cache", kpe_cache),
+                 ("out", out)):
+        _check_cuda(n, t, torch.bfloat16)
+    for n, t in (("kv_indptr", kv_indptr), ("kv_indices", kv_indices)):
+        _check_cuda(n, t, torch.int32)
+    _check_cuda("lse", lse, torch.float32)
+    rows, heads = q_nope.shape[0], q_nope.shape[1]
+    num_pages, page_size = _cache_geometry(ckv_cache, kpe_cache)
+    if kv_indptr.numel() - 1 != rows or out.shape != (rows, heads, HEAD_DIM_CKV) or lse.shape != (rows, heads):
+        raise ValueError("shape mismatch between q_nope, kv_indptr, out and lse")
+    dims = make_dims(rows, heads, num_pages, page_size, kv_indices.numel(), num_workers=num_workers)
+    if stream is None:
+        stream = torch.cuda.current_stream(q_nope.device)
+    with torch.cuda.device(q_nope.device):
+        st = lib().mla_paged_decode_noalloc(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                            _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out),
+                                            _ptr(lse), ctypes.byref(dims), 0, ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise MlaError(st, "mla_paged_decode_noalloc")
+    return out, lse
 
 
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:
