@@ -14,18 +14,21 @@
 // O[:, 256r : 256r+256] and a 288-wide slice of the 576-wide query-key depth:
 //   rank r: ckv[:, 256r : 256r+256] (its V columns too) and kpe[:, 32r : 32r+32].
 // Each CTA computes a partial S over its depth slice; the two partial S tiles are
-// swapped through distributed shared memory (st.async) and added, so every score is
-// computed once and both CTAs see identical S (fp32 addition commutes), hence take
-// identical softmax decisions.  This is the left/right split of the output that
+// swapped through distributed shared memory and added, so every score is computed
+// once.  The partials travel as 24-bit floats (fp32 rounded to 16 mantissa bits,
+// relative error <= 2^-17, 24 KB per 64-key tile instead of 32 KB): the SM-to-SM network
+// was measured at ~31 GB/s per SM each way, so the exchange volume, not the MMA work,
+// bounds this design.  Both CTAs add the same rounded values (fp32 addition commutes),
+// so they see identical S and take identical softmax decisions.  This is the left/right split of the output that
 // FlashMLA's "seesaw" schedule uses across two warpgroups (oL, oR), done here across
 // the two SMs of a cluster with the depth split as well.
 //
 // Tensor memory (496 of 512 columns): O half (256 fp32), S (64 fp32), P (32 columns
 // of packed bf16 pairs) and this CTA's Q slice (144 columns of bf16 pairs), so both
 // products read one operand from TMEM: S = Q.K^T and O += P.V are TS-form tcgen05.mma.
-// Shared memory: a 3-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
-// 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 32 KB)
-// that the peer fills, one 32 KB staging buffer for the outgoing partial (sent with a
+// Shared memory: a 4-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
+// 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 24 KB)
+// that the peer fills, one 24 KB staging buffer for the outgoing partial (sent with a
 // shared::cta -> shared::cluster bulk copy), and small reduction buffers.
 //
 // Warp roles (352 threads per CTA):
@@ -61,12 +64,12 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;    // issues S = Q.K^T; owns TMEM
 constexpr int kPvWarp = 10;    // issues O += P.V
 constexpr int kThreads = 352;
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kChunkPe = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
 constexpr uint32_t kStageBytes = 4 * kChunkKV + kChunkPe;
-constexpr uint32_t kXBytes = 128 * 64 * 4;  // one partial-S tile, fp32
+constexpr uint32_t kXBytes = 128 * 64 * 3;  // one partial-S tile, 24-bit floats
 constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffX = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kOffOut = kOffX + 2 * kXBytes;  // outgoing partial S (staging for the bulk copy)
@@ -103,6 +106,25 @@ static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
 // All eight softmax warps.
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 5, 256;" ::: "memory"); }
+
+// Partial scores cross between the two CTAs as 24-bit floats: the fp32 value rounded
+// to nearest at 16 mantissa bits (relative error <= 2^-17), four values in three words.
+// Both CTAs add the rounded values, so their scores stay bitwise identical.
+__device__ __forceinline__ uint32_t round24(uint32_t f) { return (f + 0x80u) & 0xFFFFFF00u; }
+
+__device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {  // v[4] rounded -> w[3]
+  const uint32_t t0 = v[0] >> 8, t1 = v[1] >> 8, t2 = v[2] >> 8, t3 = v[3] >> 8;
+  w[0] = t0 | (t1 << 24);
+  w[1] = (t1 >> 8) | (t2 << 16);
+  w[2] = (t2 >> 16) | (t3 << 8);
+}
+
+__device__ __forceinline__ void unpack24(const uint32_t* w, float* x) {  // w[3] -> x[4]
+  x[0] = __uint_as_float(w[0] << 8);
+  x[1] = __uint_as_float(((w[0] >> 24) | (w[1] << 8)) << 8);
+  x[2] = __uint_as_float(((w[1] >> 16) | (w[2] << 16)) << 8);
+  x[3] = __uint_as_float((w[2] >> 8) << 8);
+}
 
 __device__ __forceinline__ void pair_sync(int warp) {
   // The two softmax warps that serve the same TMEM lanes (w and w + 4).
@@ -432,6 +454,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
       tmem_ld_wait();
+#pragma unroll
+      for (int k = 0; k < 32; ++k) sn[k] = round24(sn[k]);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(S_EMPTY));
@@ -453,12 +477,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t b = jf & 1;
       if (threadIdx.x == 0) bulk_wait_group_read0();
       softmax_sync();
+      // 32 rounded scores -> 24 words -> six 16-byte chunks; chunk c of (row, half) at
+      // ((6 * half + c) * 128 + row) * 16 (a warp writes 512 contiguous bytes).
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t a = out_local + ((8 * half + c) * 128 + row) * 16;
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(sn[4 * c]), "r"(sn[4 * c + 1]),
-                     "r"(sn[4 * c + 2]), "r"(sn[4 * c + 3])
-                     : "memory");
+      for (int hh = 0; hh < 2; ++hh) {  // 16 scores -> 12 words -> 3 chunks at a time
+        uint32_t wds[12];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) pack24(&sn[16 * hh + 4 * g], &wds[3 * g]);
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const uint32_t a = out_local + ((6 * half + 3 * hh + c) * 128 + row) * 16;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wds[4 * c]), "r"(wds[4 * c + 1]),
+                       "r"(wds[4 * c + 2]), "r"(wds[4 * c + 3])
+                       : "memory");
+        }
       }
       fence_proxy_async_smem();
       softmax_sync();
@@ -485,14 +517,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t b = j & 1;
       if (!mbar_wait<true>(bar(X_FULL0 + b), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
       float s[32];
-      const float4* xin = reinterpret_cast<const float4*>(smem + kOffX + b * kXBytes);
+      const uint4* xin = reinterpret_cast<const uint4*>(smem + kOffX + b * kXBytes);
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const float4 v = xin[(8 * half + c) * 128 + row];
-        s[4 * c + 0] = __uint_as_float(sn[4 * c + 0]) + v.x;
-        s[4 * c + 1] = __uint_as_float(sn[4 * c + 1]) + v.y;
-        s[4 * c + 2] = __uint_as_float(sn[4 * c + 2]) + v.z;
-        s[4 * c + 3] = __uint_as_float(sn[4 * c + 3]) + v.w;
+      for (int hh = 0; hh < 2; ++hh) {  // 3 chunks -> 12 words -> 16 scores at a time
+        uint32_t wds[12];
+#pragma unroll
+        for (int c = 0; c < 3; ++c) {
+          const uint4 v = xin[(6 * half + 3 * hh + c) * 128 + row];
+          wds[4 * c + 0] = v.x;
+          wds[4 * c + 1] = v.y;
+          wds[4 * c + 2] = v.z;
+          wds[4 * c + 3] = v.w;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          float peer_s[4];
+          unpack24(&wds[3 * g], peer_s);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) s[16 * hh + 4 * g + e] = __uint_as_float(sn[16 * hh + 4 * g + e]) + peer_s[e];
+        }
       }
       if (threadIdx.x == 0) mbar_arrive_expect_tx(bar(X_FULL0 + b), kXBytes);  // arm its next use
       // Tile j+1's scores leave for the peer only after buffer b has been read (see
