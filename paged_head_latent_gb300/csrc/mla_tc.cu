@@ -16,20 +16,27 @@
 // Each CTA computes a partial S over its depth slice; the two partial S tiles are
 // swapped through distributed shared memory and added, so every score is computed
 // once.  The partials travel as 24-bit floats (fp32 rounded to 16 mantissa bits,
-// relative error <= 2^-17, 24 KB per 64-key tile instead of 32 KB): the SM-to-SM network
-// was measured at ~31 GB/s per SM each way, so the exchange volume, not the MMA work,
-// bounds this design.  Both CTAs add the same rounded values (fp32 addition commutes),
-// so they see identical S and take identical softmax decisions.  This is the left/right split of the output that
+// relative error <= 2^-17, 24 KB per 64-key tile instead of 32 KB).  Both CTAs add the
+// same rounded values (fp32 addition commutes), so they see identical S and take
+// identical softmax decisions.  This is the left/right split of the output that
 // FlashMLA's "seesaw" schedule uses across two warpgroups (oL, oR), done here across
 // the two SMs of a cluster with the depth split as well.
+//
+// The exchange is the pair's critical path: a one-way SM-to-SM transfer was measured at
+// over a microsecond inside this kernel, about as long as a tile's HBM time.  Each
+// softmax warp exchanges its own 3 KB piece (32 heads x 32 keys) with the warp of the
+// same index in the peer, by st.async stores straight from registers that complete
+// bytes on the peer warp's mbarrier, so no warp waits for another and nothing is staged.
+// A warp sends tile j+1 as soon as it has received and read tile j; flow control is
+// implicit (the peer sent tile j only after reading tile j-1 from the buffer that tile
+// j+1 goes to), so two buffers per warp suffice.
 //
 // Tensor memory (496 of 512 columns): O half (256 fp32), S (64 fp32), P (32 columns
 // of packed bf16 pairs) and this CTA's Q slice (144 columns of bf16 pairs), so both
 // products read one operand from TMEM: S = Q.K^T and O += P.V are TS-form tcgen05.mma.
 // Shared memory: a 4-stage ring of 64-key tiles (4 x 8 KB of ckv in 128-byte swizzle,
 // 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 24 KB)
-// that the peer fills, one 24 KB staging buffer for the outgoing partial (sent with a
-// shared::cta -> shared::cluster bulk copy), and small reduction buffers.
+// that the peer fills, and small reduction buffers.
 //
 // Warp roles (352 threads per CTA):
 //   warps 0-7  softmax / correction / epilogue / Q loading.  Warp w serves TMEM lanes
@@ -37,7 +44,7 @@
 //              each tile; the two warps of a lane group combine their row maxima through
 //              shared memory and a 64-thread named barrier.  The loop is software
 //              pipelined: tile j+1's partial S leaves for the peer before tile j's
-//              softmax runs.
+//              softmax runs, and tile j+2's S is being computed meanwhile.
 //   warp 8     TMA producer: one box load per column chunk when the tile's 64 slots
 //              are contiguous (a whole page of 64), else tile::gather4 row loads; rows
 //              past the row's length read a slot outside the cache, which TMA fills
@@ -45,9 +52,6 @@
 //   warp 9     issues S = Q.K^T (one thread) and owns TMEM
 //   warp 10    issues O += P.V (one thread); tcgen05.mma issue blocks while the tensor
 //              pipe is busy, so the two products get separate issuing threads.
-// The exchange needs no "buffer free" signal: the peer refills buffer b with tile
-// j+2 only after it has received this CTA's tile j+1, which each thread sends after
-// it has read tile j from buffer b.
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -72,13 +76,13 @@ constexpr uint32_t kStageBytes = 4 * kChunkKV + kChunkPe;
 constexpr uint32_t kXBytes = 128 * 64 * 3;  // one partial-S tile, 24-bit floats
 constexpr uint32_t kOffKV = 0;
 constexpr uint32_t kOffX = kOffKV + kStages * kStageBytes;
-constexpr uint32_t kOffOut = kOffX + 2 * kXBytes;  // outgoing partial S (staging for the bulk copy)
-constexpr uint32_t kOffRed = kOffOut + kXBytes;    // [2][2][128] row maxima
+constexpr uint32_t kXWarpBytes = kXBytes / 8;  // one softmax warp's piece: 32 rows x 32 keys
+constexpr uint32_t kOffRed = kOffX + 2 * kXBytes;  // [2][2][128] row maxima
 constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;  // [2][128] row sums
 constexpr uint32_t kOffDesc = kOffL + 2 * 128 * 4;  // ring of kDescRing tile descriptors
 constexpr int kDescRing = 8;
 constexpr uint32_t kOffBar = kOffDesc + kDescRing * 32;
-constexpr uint32_t kOffMisc = kOffBar + 256;
+constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColO = 0;    // 256 columns
@@ -89,7 +93,7 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by mo
 
 enum Bar : uint32_t {
   Q_FULL, KV_FULL0, KV_EMPTY0 = KV_FULL0 + kStages, S_FULL = KV_EMPTY0 + kStages, S_EMPTY, P_FULL, PV_DONE,
-  X_FULL0, X_FULL1, O_FULL, O_EMPTY, DRAIN, NUM_BARS
+  X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, NUM_BARS
 };
 
 struct Misc {
@@ -99,13 +103,10 @@ struct Misc {
   Cursor cur;
 };
 
-static_assert(NUM_BARS * 8 <= 256, "barrier area");
+static_assert(NUM_BARS * 8 <= 512, "barrier area");
 static_assert(sizeof(Misc) <= 64, "misc area");
 static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
-
-// All eight softmax warps.
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 5, 256;" ::: "memory"); }
 
 // Partial scores cross between the two CTAs as 24-bit floats: the fp32 value rounded
 // to nearest at 16 mantissa bits (relative error <= 2^-17), four values in three words.
@@ -205,15 +206,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(S_EMPTY), kSoftmaxWarps);
     mbar_init(bar(P_FULL), kSoftmaxWarps);
     mbar_init(bar(PV_DONE), 1);
-    mbar_init(bar(X_FULL0), 1);
-    mbar_init(bar(X_FULL1), 1);
+    for (int i = 0; i < 16; ++i) mbar_init(bar(X_FULL0 + i), 1);  // [buffer][softmax warp]
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), kSoftmaxWarps);
     mbar_init(bar(DRAIN), 2);  // one commit from each MMA-issuing thread
     fence_mbar_init();
-    // Arm the first phase of both exchange barriers before the peer can send.
-    mbar_arrive_expect_tx(bar(X_FULL0), kXBytes);
-    mbar_arrive_expect_tx(bar(X_FULL1), kXBytes);
+    // Arm the first phase of every exchange barrier before the peer can send.
+    for (int i = 0; i < 16; ++i) mbar_arrive_expect_tx(bar(X_FULL0 + i), kXWarpBytes);
   }
   if (warp == kMmaWarp) {
     tmem_alloc(sbase + kOffMisc, kTmemCols);  // misc.tmem is the first word of Misc
@@ -396,8 +395,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t x_local = sbase + kOffX;
     const uint32_t x_remote = mapa(x_local, peer);
-    const uint32_t xfull_remote0 = mapa(bar(X_FULL0), peer);
-    const uint32_t xfull_remote1 = mapa(bar(X_FULL1), peer);
+    // Exchange piece of this warp: [buffer][warp][chunk c][lane] 16-byte units, the
+    // same layout on both CTAs, so warp w of one CTA sends only to warp w of the other.
+    const uint32_t piece = warp * kXWarpBytes + lane * 16;
+    const uint32_t xfull_remote = mapa(bar(X_FULL0 + warp), peer);    // + 64 * buffer
     float* red = reinterpret_cast<float*>(smem + kOffRed);
     float* lbuf = reinterpret_cast<float*>(smem + kOffL);
     const float scale = p.scale_log2;
@@ -445,17 +446,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
     const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
     bool ok = true;
-    uint32_t jf = 0;  // tiles fetched
-    uint32_t sn[32];  // partial scores of the last fetched tile
-    // Fetch tile jf, part 1: read its partial S from TMEM, release S, and write the
-    // next segment's Q slice if this was the segment's last QK.
-    auto fetch_scores = [&]() -> bool {
+    uint32_t jf = 0;       // tiles fetched
+    uint32_t nxt[24];      // own partial scores of tile jf - 1, rounded and packed
+    // Fetch tile jf: read its partial S from TMEM, release S, round and pack it, and
+    // write the next segment's Q slice if this was the segment's last QK.
+    auto fetch = [&]() -> bool {
       if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout)) return false;
       tc_fence_after();
-      tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
-      tmem_ld_wait();
+      {
+        uint32_t sn[32];
+        tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
+        tmem_ld_wait();
 #pragma unroll
-      for (int k = 0; k < 32; ++k) sn[k] = round24(sn[k]);
+        for (int g = 0; g < 8; ++g) {
+          uint32_t v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = round24(sn[4 * g + e]);
+          pack24(v, &nxt[3 * g]);
+        }
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(S_EMPTY));
@@ -464,86 +473,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return false;
       const int next_row = desc[jf % kDescRing].next_row;
       if (next_row >= 0) write_q(next_row);
+      ++jf;
       return true;
     };
-    // Part 2: send the partial to the peer's exchange buffer jf & 1.  The threads stage
-    // it in their own shared memory (16-byte chunk c of row r at (c * 128 + r) * 16, the
-    // peer's layout) and one thread hands the 32 KB to the bulk-copy engine, so the
-    // transfer runs in the background of the softmax.  The staging buffer is rewritten
-    // only after the previous bulk copy has read it (wait_group.read before the first
-    // barrier).
-    const uint32_t out_local = sbase + kOffOut;
-    auto send_scores = [&]() {
-      const uint32_t b = jf & 1;
-      if (threadIdx.x == 0) bulk_wait_group_read0();
-      softmax_sync();
-      // 32 rounded scores -> 24 words -> six 16-byte chunks; chunk c of (row, half) at
-      // ((6 * half + c) * 128 + row) * 16 (a warp writes 512 contiguous bytes).
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // 16 scores -> 12 words -> 3 chunks at a time
-        uint32_t wds[12];
-#pragma unroll
-        for (int g = 0; g < 4; ++g) pack24(&sn[16 * hh + 4 * g], &wds[3 * g]);
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          const uint32_t a = out_local + ((6 * half + 3 * hh + c) * 128 + row) * 16;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(wds[4 * c]), "r"(wds[4 * c + 1]),
-                       "r"(wds[4 * c + 2]), "r"(wds[4 * c + 3])
-                       : "memory");
-        }
-      }
-      fence_proxy_async_smem();
-      softmax_sync();
-      if (threadIdx.x == 0) {
-        bulk_copy_to_peer(x_remote + b * kXBytes, out_local, kXBytes, b ? xfull_remote1 : xfull_remote0);
-        bulk_commit_group();
-      }
-      ++jf;
-    };
 
+    // Send this warp's piece of tile t (the packed own partial v) into the peer warp's
+    // exchange buffer t & 1; the stores complete their bytes on the peer warp's X_FULL
+    // barrier of that buffer.  Flow control is implicit: the piece of tile t + 1 leaves
+    // only after this warp has received the peer's piece of tile t, which the peer sent
+    // after it had read (and re-armed) its buffer (t + 1) & 1 for tile t - 1.
+    auto send_piece = [&](uint32_t t, const uint32_t (&v)[24]) {
+      const uint32_t dst = x_remote + (t & 1) * kXBytes + piece;
+#pragma unroll
+      for (int c = 0; c < 6; ++c)
+        st_async_v4(dst + c * 512, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], xfull_remote + 64 * (t & 1));
+    };
     if (ntiles > 0) {
       if (!mbar_wait(bar(KV_FULL0), 0, abort, p.status, kStatusTimeout)) {
         ok = false;
       } else {
         write_q(desc[0].row);
-        ok = fetch_scores();
-        if (ok) send_scores();
+        ok = fetch();
+        if (ok) send_piece(0, nxt);
       }
     }
     float m_ref = -INFINITY, l = 0.f;  // l: this thread's 32 columns only
     uint32_t j = 0;
     while (ok && j < jf) {
-      const TileDesc cd = desc[j % kDescRing];  // tile j (KV_FULL seen in fetch_scores)
+      const TileDesc cd = desc[j % kDescRing];  // tile j (KV_FULL seen in fetch)
       const uint32_t b = j & 1;
-      if (!mbar_wait<true>(bar(X_FULL0 + b), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
+      uint32_t own[24];  // own partial of tile j
+#pragma unroll
+      for (int i = 0; i < 24; ++i) own[i] = nxt[i];
+      // Tile j+1's partial is fetched before this warp waits for tile j's piece, so it
+      // can leave the moment tile j's has arrived.
+      if (jf < ntiles && !fetch()) break;
+      if (!mbar_wait<true>(bar(X_FULL0 + 8 * b + warp), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
       float s[32];
-      const uint4* xin = reinterpret_cast<const uint4*>(smem + kOffX + b * kXBytes);
+      {
+        uint32_t pw[24];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // 3 chunks -> 12 words -> 16 scores at a time
-        uint32_t wds[12];
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          const uint4 v = xin[(6 * half + 3 * hh + c) * 128 + row];
-          wds[4 * c + 0] = v.x;
-          wds[4 * c + 1] = v.y;
-          wds[4 * c + 2] = v.z;
-          wds[4 * c + 3] = v.w;
+        for (int c = 0; c < 6; ++c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffX + b * kXBytes + piece + c * 512);
+          pw[4 * c] = v.x;
+          pw[4 * c + 1] = v.y;
+          pw[4 * c + 2] = v.z;
+          pw[4 * c + 3] = v.w;
         }
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          float peer_s[4];
-          unpack24(&wds[3 * g], peer_s);
+        for (int g = 0; g < 8; ++g) {
+          float a[4], c4[4];
+          unpack24(&own[3 * g], a);
+          unpack24(&pw[3 * g], c4);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[16 * hh + 4 * g + e] = __uint_as_float(sn[16 * hh + 4 * g + e]) + peer_s[e];
+          for (int e = 0; e < 4; ++e) s[4 * g + e] = a[e] + c4[e];
         }
       }
-      if (threadIdx.x == 0) mbar_arrive_expect_tx(bar(X_FULL0 + b), kXBytes);  // arm its next use
-      // Tile j+1's scores leave for the peer only after buffer b has been read (see
-      // the header), and before tile j's softmax runs.
-      if (jf < ntiles) {
-        if (!fetch_scores()) break;
-        send_scores();
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(bar(X_FULL0 + 8 * b + warp), kXWarpBytes);  // arm its next use
+      __syncwarp();
+      if (jf > j + 1) send_piece(j + 1, nxt);  // then send tile j+1
       const int nvalid = min(kTileKeys, cd.len - cd.t * kTileKeys) - 32 * half;
       float mx = -INFINITY;
 #pragma unroll
@@ -651,7 +640,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (threadIdx.x == 0) bulk_wait_group_read0();  // no bulk copy may still read our smem
   tc_fence_before();
   __syncthreads();
   cluster_sync();
