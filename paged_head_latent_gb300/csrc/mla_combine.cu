@@ -18,7 +18,8 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 __device__ __forceinline__ long long frag_index(const CombineRecord& rec, int f, int G) {
   const int wk = rec.w_first + f;
   const long long T = rec.total_tiles;
-  if (worker_start(wk + 1, T, G) == worker_start(wk, T, G)) return -1;
+  // Every worker has at least one tile when T >= G, so the division is needed only below.
+  if (T < G && worker_start(wk + 1, T, G) == worker_start(wk, T, G)) return -1;
   return (long long)wk * 2 + (f == 0 ? rec.slot_first : 0);
 }
 

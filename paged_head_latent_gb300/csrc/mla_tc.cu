@@ -93,7 +93,7 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by mo
 
 enum Bar : uint32_t {
   Q_FULL, KV_FULL0, KV_EMPTY0 = KV_FULL0 + kStages, S_FULL = KV_EMPTY0 + kStages, S_EMPTY, P_FULL, PV_DONE,
-  X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, NUM_BARS
+  X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, DESC0, NUM_BARS
 };
 
 struct Misc {
@@ -210,6 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(O_FULL), 1);
     mbar_init(bar(O_EMPTY), kSoftmaxWarps);
     mbar_init(bar(DRAIN), 2);  // one commit from each MMA-issuing thread
+    mbar_init(bar(DESC0), 1);  // the first tile's descriptor is written
     fence_mbar_init();
     // Arm the first phase of every exchange barrier before the peer can send.
     for (int i = 0; i < 16; ++i) mbar_arrive_expect_tx(bar(X_FULL0 + i), kXWarpBytes);
@@ -225,6 +226,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       misc.cur = c;
       misc.T = T;
+      // Start pulling the first query row into L2 now; the softmax warps read it into
+      // TMEM as soon as the first tile's descriptor exists.  (If that row turns out to
+      // have no keys, the prefetch was merely useless.)
+      if (T > 0 && c.b < p.batch) {
+        const int row = p.qo_indptr ? __ldg(p.qo_indptr + c.b) + c.i : c.b;
+        if (row >= 0 && row < p.rows) {
+          if (rank == 0) bulk_prefetch_l2(p.q_nope + (size_t)row * p.heads * kDimCkv, p.heads * kDimCkv * 2);
+          else bulk_prefetch_l2(p.q_pe + (size_t)row * p.heads * kDimKpe, p.heads * kDimKpe * 2);
+        }
+      }
     }
     if (w == 0 && rank == 0) warp_write_empty_rows(p);
   }
@@ -300,6 +311,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (peek.live) d.next_row = peek.seg.row;
         }
         desc[j % kDescRing] = d;
+        if (j == 0) mbar_arrive(bar(DESC0));       // lets the softmax warps load Q early
         mbar_arrive_expect_tx(kvbar, kStageBytes);  // release: orders the descriptor before the tile
       }
       __syncwarp();
@@ -489,7 +501,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         st_async_v4(dst + c * 512, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], xfull_remote + 64 * (t & 1));
     };
     if (ntiles > 0) {
-      if (!mbar_wait(bar(KV_FULL0), 0, abort, p.status, kStatusTimeout)) {
+      if (!mbar_wait(bar(DESC0), 0, abort, p.status, kStatusTimeout)) {
         ok = false;
       } else {
         write_q(desc[0].row);
