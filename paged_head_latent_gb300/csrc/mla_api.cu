@@ -10,7 +10,6 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -164,15 +163,6 @@ int build_maps(const MlaParams& p, mla::TmaMaps* m) {
   return MLA_OK;
 }
 
-bool force_simt() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = std::getenv("MLA_FORCE_SIMT");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
-  return v == 1;
-}
-
 // ---------------------------------------------------------------- profiling
 struct ProfileState {
   bool on = false;
@@ -253,9 +243,7 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   }
   cudaEvent_t* ev = profile_slot();
   if (ev) cudaEventRecord(ev[0], stream);
-  if (force_simt()) {
-    if (mla::launch_simt(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
-  } else {
+  {
     mla::TmaMaps maps;
     st = build_maps(p, &maps);
     if (st != MLA_OK) return st;
