@@ -53,13 +53,17 @@ def algorithmic_work(w):
     return nbytes, flops, keys
 
 
+# The sources that define the attention kernel and its launch (tensor-map shapes); the
+# recorded DRAM traffic is valid only while these are unchanged.
+KERNEL_SOURCES = ("mla_tc.cu", "tc_kernel.h", "ptx.cuh", "plan.cuh", "common.cuh", "launch.h", "mla_api.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_head_latent_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode() + f.read())
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 
@@ -171,6 +175,16 @@ def cores_used():
         return os.cpu_count()
 
 
+def max_over_ranks(value, world, device=None):
+    """The largest value over all ranks (every rank gets it); the value itself at N = 1."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def reference_arm(args, rank, world):
     from paged_head_latent_gb300 import workloads as wl
     if rank != 0:
@@ -264,11 +278,7 @@ def our_arm(args, rank, world, local_rank):
     main_ms, comb_ms, ncalls = mla.profile_read()
     mla.profile_enable(False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_per_step = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     main_avg_ms = main_ms / max(ncalls, 1)
     comb_avg_ms = comb_ms / max(ncalls, 1)
 
@@ -294,11 +304,7 @@ def our_arm(args, rank, world, local_rank):
         if e2e_steps:
             e1.record(stream)
     stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan")
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan"), world, dev)
 
     if rank != 0:
         return
