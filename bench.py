@@ -53,9 +53,9 @@ def algorithmic_work(w):
     return nbytes, flops, keys
 
 
-# The sources that define the attention kernel and its launch (tensor-map shapes); the
-# recorded DRAM traffic is valid only while these are unchanged.
-KERNEL_SOURCES = ("mla_tc.cu", "tc_kernel.h", "ptx.cuh", "plan.cuh", "common.cuh", "launch.h", "mla_api.cu")
+# The sources that define the attention kernel; the recorded DRAM traffic is valid only
+# while these are unchanged.
+KERNEL_SOURCES = ("mla_tc.cu", "tc_kernel.h", "ptx.cuh", "plan.cuh", "common.cuh")
 
 
 def kernel_source_hash():
