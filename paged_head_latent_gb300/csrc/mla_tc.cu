@@ -15,8 +15,8 @@
 //   rank r: ckv[:, 256r : 256r+256] (its V columns too) and kpe[:, 32r : 32r+32].
 // Each CTA computes a partial S over its depth slice; the two partial S tiles are
 // swapped through distributed shared memory and added, so every score is computed
-// once.  The partials travel as 24-bit floats (fp32 rounded to 16 mantissa bits,
-// relative error <= 2^-17, 24 KB per 64-key tile instead of 32 KB).  Both CTAs add the
+// once.  The partials travel as 24-bit floats (fp32 rounded to 16 significant bits,
+// relative error <= 2^-16, 24 KB per 64-key tile instead of 32 KB).  Both CTAs add the
 // same rounded values (fp32 addition commutes), so they see identical S and take
 // identical softmax decisions.  This is the left/right split of the output that
 // FlashMLA's "seesaw" schedule uses across two warpgroups (oL, oR), done here across
@@ -109,22 +109,23 @@ static_assert(kSmemBytes <= 232448, "shared memory");
 static_assert(kStageBytes % 1024 == 0, "stage alignment");
 
 // Partial scores cross between the two CTAs as 24-bit floats: the fp32 value rounded
-// to nearest at 16 mantissa bits (relative error <= 2^-17), four values in three words.
+// to nearest at 16 significant bits (relative error <= 2^-16), four values in three words.
 // Both CTAs add the rounded values, so their scores stay bitwise identical.
-__device__ __forceinline__ uint32_t round24(uint32_t f) { return (f + 0x80u) & 0xFFFFFF00u; }
+// round24: add half of the dropped byte (a carry rounds up into the exponent); pack24
+// then keeps the top three bytes of each value, so the pair rounds to nearest.
+__device__ __forceinline__ uint32_t round24(uint32_t f) { return f + 0x80u; }
 
-__device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {  // v[4] rounded -> w[3]
-  const uint32_t t0 = v[0] >> 8, t1 = v[1] >> 8, t2 = v[2] >> 8, t3 = v[3] >> 8;
-  w[0] = t0 | (t1 << 24);
-  w[1] = (t1 >> 8) | (t2 << 16);
-  w[2] = (t2 >> 16) | (t3 << 8);
+__device__ __forceinline__ void pack24(const uint32_t* v, uint32_t* w) {  // v[4] -> w[3], byte permutes
+  w[0] = __byte_perm(v[0], v[1], 0x5321);  // v0.b1 v0.b2 v0.b3 v1.b1
+  w[1] = __byte_perm(v[1], v[2], 0x6532);  // v1.b2 v1.b3 v2.b1 v2.b2
+  w[2] = __byte_perm(v[2], v[3], 0x7653);  // v2.b3 v3.b1 v3.b2 v3.b3
 }
 
-__device__ __forceinline__ void unpack24(const uint32_t* w, float* x) {  // w[3] -> x[4]
-  x[0] = __uint_as_float(w[0] << 8);
-  x[1] = __uint_as_float(((w[0] >> 24) | (w[1] << 8)) << 8);
-  x[2] = __uint_as_float(((w[1] >> 16) | (w[2] << 16)) << 8);
-  x[3] = __uint_as_float((w[2] >> 8) << 8);
+__device__ __forceinline__ void unpack24(const uint32_t* w, float* x) {  // w[3] -> x[4], low bytes zero
+  x[0] = __uint_as_float(__byte_perm(w[0], 0u, 0x2104));
+  x[1] = __uint_as_float(__funnelshift_r(w[0], w[1], 16) & 0xFFFFFF00u);
+  x[2] = __uint_as_float(__funnelshift_r(w[1], w[2], 8) & 0xFFFFFF00u);
+  x[3] = __uint_as_float(__byte_perm(w[2], 0u, 0x3214));
 }
 
 __device__ __forceinline__ void pair_sync(int warp) {
@@ -546,11 +547,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (jf > j + 1) send_piece(j + 1, nxt);  // then send tile j+1
       const int nvalid = min(kTileKeys, cd.len - cd.t * kTileKeys) - 32 * half;
+      // All 32 keys valid and a non-negative scale (the usual case): the maximum of the
+      // scaled scores is the scaled maximum, and the scale folds into the exponent below.
+      const bool full = nvalid >= 32 && scale >= 0.f;
       float mx = -INFINITY;
+      if (full) {
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        s[k] = k < nvalid ? s[k] * scale : -INFINITY;
-        mx = fmaxf(mx, s[k]);
+        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, s[k]);
+        mx *= scale;
+      } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = k < nvalid ? s[k] * scale : -INFINITY;
+          mx = fmaxf(mx, s[k]);
+        }
       }
       red[(b * 2 + half) * 128 + row] = mx;
       pair_sync(warp);
@@ -568,13 +578,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       uint32_t pk[16];
       float sum = 0.f;
+      if (full) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const float a = fast_exp2(s[2 * k] - m_ref);
-        const float bb = fast_exp2(s[2 * k + 1] - m_ref);
-        sum += a + bb;
-        __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
-        pk[k] = *reinterpret_cast<uint32_t*>(&h);
+        for (int k = 0; k < 16; ++k) {
+          const float a = fast_exp2(fmaf(s[2 * k], scale, -m_ref));
+          const float bb = fast_exp2(fmaf(s[2 * k + 1], scale, -m_ref));
+          sum += a + bb;
+          __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
+          pk[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float a = fast_exp2(s[2 * k] - m_ref);
+          const float bb = fast_exp2(s[2 * k + 1] - m_ref);
+          sum += a + bb;
+          __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
+          pk[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
       }
       l += sum;
       // P is single-buffered: the previous tile's P.V must be done (it also settles O).

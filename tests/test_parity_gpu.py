@@ -108,6 +108,30 @@ def test_decode_long_request_last(lib):
     check_full(lib, w)
 
 
+@pytest.mark.parametrize("sm_scale", [0.0, -0.05, 0.5])
+def test_decode_unusual_scales(lib, sm_scale):
+    """Zero scale (uniform weights), a negative scale and a large one (peaked rows), with
+    tails that leave tiles partly empty."""
+    w = dataclasses.replace(wl.make_decode([1, 63, 65, 200, 777], num_qo_heads=128, page_size=64, seed=2304),
+                            sm_scale=sm_scale)
+    check_full(lib, w)
+
+
+def test_decode_dominant_key(lib):
+    """One key per request lines up with head 0's query, so that head's softmax puts all
+    its weight on that key (its score is ~20 above the rest): lse must track that
+    single score to the tolerance."""
+    w = wl.make_decode([300, 64, 1000], num_qo_heads=128, page_size=64, seed=2305)
+    ckv = w.ckv_cache.clone().view(-1, 512)
+    kpe = w.kpe_cache.clone().view(-1, 64)
+    for b in range(w.batch):
+        slot = int(w.kv_indices[int(w.kv_indptr[b]) + 17 % max(1, int(w.kv_indptr[b + 1] - w.kv_indptr[b]))])
+        ckv[slot] = (w.q_nope[b, 0].float() * 0.5).to(torch.bfloat16)
+        kpe[slot] = (w.q_pe[b, 0].float() * 0.5).to(torch.bfloat16)
+    w = dataclasses.replace(w, ckv_cache=ckv.view_as(w.ckv_cache), kpe_cache=kpe.view_as(w.kpe_cache))
+    check_full(lib, w)
+
+
 # -------------------------------------------------------------- small prefill
 
 @pytest.mark.parametrize("q_lens,prefixes,heads,ps", [
