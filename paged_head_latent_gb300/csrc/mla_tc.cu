@@ -309,7 +309,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (it.last()) {
           TileIter peek = it;
           peek.advance();
-          if (peek.live) d.next_row = peek.seg.row;
+          if (peek.live) {
+            d.next_row = peek.seg.row;
+            // The softmax warps load that row's Q into TMEM once this tile's QK is done,
+            // a few tiles from now; pull it into L2 meanwhile.
+            const size_t r = (size_t)d.next_row * p.heads;
+            if (rank == 0) bulk_prefetch_l2(p.q_nope + r * kDimCkv, p.heads * kDimCkv * 2);
+            else bulk_prefetch_l2(p.q_pe + r * kDimKpe, p.heads * kDimKpe * 2);
+          }
         }
         desc[j % kDescRing] = d;
         if (j == 0) mbar_arrive(bar(DESC0));       // lets the softmax warps load Q early
@@ -461,8 +468,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t jf = 0;       // tiles fetched
     uint32_t nxt[24];      // own partial scores of tile jf - 1, rounded and packed
-    // Fetch tile jf: read its partial S from TMEM, release S, round and pack it, and
-    // write the next segment's Q slice if this was the segment's last QK.
+    // Fetch tile jf: read its partial S from TMEM, release S, round and pack it, and note
+    // the next segment's row if this was the segment's last QK (its Q slice is written
+    // after this tile's piece has left for the peer, off the exchange's critical path).
+    int q_pending = -1;
     auto fetch = [&]() -> bool {
       if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout)) return false;
       tc_fence_after();
@@ -484,8 +493,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // The tile's descriptor: its KV_FULL phase has completed (QK read the tile).
       if (!mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout))
         return false;
-      const int next_row = desc[jf % kDescRing].next_row;
-      if (next_row >= 0) write_q(next_row);
+      q_pending = desc[jf % kDescRing].next_row;
       ++jf;
       return true;
     };
@@ -508,6 +516,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         write_q(desc[0].row);
         ok = fetch();
         if (ok) send_piece(0, nxt);
+        if (ok && q_pending >= 0) {
+          write_q(q_pending);
+          q_pending = -1;
+        }
       }
     }
     float m_ref = -INFINITY, l = 0.f;  // l: this thread's 32 columns only
@@ -545,7 +557,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(bar(X_FULL0 + 8 * b + warp), kXWarpBytes);  // arm its next use
       __syncwarp();
-      if (jf > j + 1) send_piece(j + 1, nxt);  // then send tile j+1
+      if (jf > j + 1) {
+        send_piece(j + 1, nxt);  // then send tile j+1
+        if (q_pending >= 0) {
+          write_q(q_pending);
+          q_pending = -1;
+        }
+      }
       const int nvalid = min(kTileKeys, cd.len - cd.t * kTileKeys) - 32 * half;
       // All 32 keys valid and a non-negative scale (the usual case): the maximum of the
       // scaled scores is the scaled maximum, and the scale folds into the exponent below.
