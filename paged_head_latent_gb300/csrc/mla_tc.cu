@@ -79,7 +79,8 @@ constexpr uint32_t kOffX = kOffKV + kStages * kStageBytes;
 constexpr uint32_t kXWarpBytes = kXBytes / 8;  // one softmax warp's piece: 32 rows x 32 keys
 constexpr uint32_t kOffRed = kOffX + 2 * kXBytes;  // [2][2][128] row maxima
 constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;  // [2][128] row sums
-constexpr uint32_t kOffDesc = kOffL + 2 * 128 * 4;  // ring of kDescRing tile descriptors
+constexpr uint32_t kOffStg = kOffL + 2 * 128 * 4;  // [softmax warp] 2 KB: Q in / O out transposes
+constexpr uint32_t kOffDesc = kOffStg + 8 * 2048;  // ring of kDescRing tile descriptors
 constexpr int kDescRing = 8;
 constexpr uint32_t kOffBar = kOffDesc + kDescRing * 32;
 constexpr uint32_t kOffMisc = kOffBar + 512;
@@ -127,6 +128,12 @@ __device__ __forceinline__ void unpack24(const uint32_t* w, float* x) {  // w[3]
   x[2] = __uint_as_float(__funnelshift_r(w[1], w[2], 8) & 0xFFFFFF00u);
   x[3] = __uint_as_float(__byte_perm(w[2], 0u, 0x3214));
 }
+
+// A warp's 2 KB transpose buffer holds 32 rows x 64 bytes: 16-byte chunk c of row r sits
+// in slot 4r + (c ^ ((r >> 1) & 3)), so both a row-per-lane access (lane r, chunks 0..3)
+// and a coalesced access (lanes 4k..4k+3 on the four chunks of one row) are free of bank
+// conflicts.
+__device__ __forceinline__ uint32_t stg_slot(int r, int c) { return 16u * (4 * r + (c ^ ((r >> 1) & 3))); }
 
 __device__ __forceinline__ void pair_sync(int warp) {
   // The two softmax warps that serve the same TMEM lanes (w and w + 4).
@@ -423,44 +430,83 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     float* lbuf = reinterpret_cast<float*>(smem + kOffL);
     const float scale = p.scale_log2;
 
-    // Write the Q slice of query row `qrow` (this thread's head, this half's columns)
-    // into TMEM: half 0 -> depth 0..127 (16 x 16 B of q_nope), half 1 -> depth
-    // 128..287 (16 x 16 B of q_nope, 4 x 16 B of q_pe).  Heads >= H get zeros.
+    // This warp's transpose buffer, and the rows (query heads) it serves.
+    const uint32_t stg = sbase + kOffStg + warp * 2048;
+    const int row0 = (warp & 3) * 32;
+
+    // Write the Q slice of query row `qrow` (this warp's heads, this half's depth) into
+    // TMEM: half 0 -> depth 0..127 (16 x 16 B of q_nope per head), half 1 -> depth
+    // 128..287 (16 x 16 B of q_nope, 4 x 16 B of q_pe).  Heads >= H get zeros.  The
+    // global reads are coalesced (each instruction reads 64 contiguous bytes of eight
+    // heads) and go through the transpose buffer to reach the thread that owns the head's
+    // TMEM lane; all of them are issued before the first is used.
     auto write_q = [&](int qrow) {
-      const bool valid = row < p.heads;
-      const size_t rg = (size_t)qrow * p.heads + row;
-      const uint4* qn = reinterpret_cast<const uint4*>(p.q_nope + rg * kDimCkv + rank * 256 + half * 128);
-      const uint4* qp = reinterpret_cast<const uint4*>(p.q_pe + rg * kDimKpe + rank * 32);
-      const uint32_t col = tmem + lane_base + kColQ + half * 64;
-      const int nvec = half ? 20 : 16;  // 16-byte pieces of this thread's slice
+      const int npass = half ? 5 : 4;  // 64-byte chunk groups per head
+      const int hh_lo = lane >> 2, cl = lane & 3;
+      uint4 v[5][4];
 #pragma unroll
-      for (int r0 = 0; r0 < 20; r0 += 8) {
-        if (r0 >= nvec) break;
-        uint4 v[8];
+      for (int ps = 0; ps < 5; ++ps) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int k = r0 + i;
-          v[i] = make_uint4(0, 0, 0, 0);
-          if (valid && k < nvec) v[i] = k < 16 ? __ldg(qn + k) : __ldg(qp + (k - 16));
-        }
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          if (r0 + 4 * c >= nvec) break;
-          uint32_t rr[16];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            rr[4 * i + 0] = v[4 * c + i].x;
-            rr[4 * i + 1] = v[4 * c + i].y;
-            rr[4 * i + 2] = v[4 * c + i].z;
-            rr[4 * i + 3] = v[4 * c + i].w;
+        for (int i = 0; i < 4; ++i) {
+          const int hh = 8 * i + hh_lo;
+          const int h = row0 + hh;
+          v[ps][i] = make_uint4(0, 0, 0, 0);
+          if (ps < npass && h < p.heads) {
+            const size_t rg = (size_t)qrow * p.heads + h;
+            const uint4* src =
+                ps < 4 ? reinterpret_cast<const uint4*>(p.q_nope + rg * kDimCkv + rank * 256 + half * 128) + 4 * ps
+                       : reinterpret_cast<const uint4*>(p.q_pe + rg * kDimKpe + rank * 32);
+            v[ps][i] = __ldg(src + cl);
           }
-          tmem_st16(col + 4 * (r0 + 4 * c), rr);  // 16 bytes = 4 columns of bf16 pairs
         }
+      }
+      const uint32_t col = tmem + lane_base + kColQ + half * 64;
+#pragma unroll
+      for (int ps = 0; ps < 5; ++ps) {
+        if (ps >= npass) break;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + stg_slot(8 * i + hh_lo, cl)),
+                       "r"(v[ps][i].x), "r"(v[ps][i].y), "r"(v[ps][i].z), "r"(v[ps][i].w)
+                       : "memory");
+        __syncwarp();
+        uint32_t rr[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(rr[4 * c]), "=r"(rr[4 * c + 1]), "=r"(rr[4 * c + 2]), "=r"(rr[4 * c + 3])
+                       : "r"(stg + stg_slot(lane, c))
+                       : "memory");
+        __syncwarp();
+        tmem_st16(col + 16 * ps, rr);  // 64 bytes = 16 columns of bf16 pairs
       }
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Q_FULL));
+    };
+
+    // Store one 16-column slice (64 bytes per head: 4 chunks per lane in c[]) of this
+    // warp's heads through the transpose buffer, so that each store instruction writes
+    // 64 contiguous bytes of eight heads.  dst(h) is the slice's address for head h.
+    auto store_rows = [&](const uint4 (&c)[4], auto dst) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + stg_slot(lane, k)), "r"(c[k].x),
+                     "r"(c[k].y), "r"(c[k].z), "r"(c[k].w)
+                     : "memory");
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int hh = 8 * i + (lane >> 2);
+        uint4 x;
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
+                     : "r"(stg + stg_slot(hh, lane & 3))
+                     : "memory");
+        if (row0 + hh < p.heads) dst(row0 + hh)[lane & 3] = x;
+      }
+      __syncwarp();
     };
 
     const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
@@ -654,26 +700,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_ld32(tmem + lane_base + kColO + 128 * half + 32 * cc, o);
           tmem_ld_wait();
           const int d0 = (int)rank * 256 + 128 * half + cc * 32;
-          if (valid) {
-            if (cd.flags & kWhole) {
-              uint4* dst = reinterpret_cast<uint4*>(p.out + ((size_t)cd.row * p.heads + row) * kDimCkv + d0);
+          if (cd.flags & kWhole) {
+            uint4 c4[4];  // 32 columns as bf16: 64 bytes
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint32_t wds[4];
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wds[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
-                                                           __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
-                  wds[e] = *reinterpret_cast<uint32_t*>(&h);
-                }
-                dst[q] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+              for (int e = 0; e < 4; ++e) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(o[8 * q + 2 * e]) * inv_l,
+                                                         __uint_as_float(o[8 * q + 2 * e + 1]) * inv_l);
+                wds[e] = *reinterpret_cast<uint32_t*>(&h);
               }
-            } else {
-              float4* dst = reinterpret_cast<float4*>(p.part_o + frag * kDimCkv + d0);
+              c4[q] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+            }
+            store_rows(c4, [&](int h) {
+              return reinterpret_cast<uint4*>(p.out + ((size_t)cd.row * p.heads + h) * kDimCkv + d0);
+            });
+          } else {
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                dst[q] = make_float4(__uint_as_float(o[4 * q]) * inv_l, __uint_as_float(o[4 * q + 1]) * inv_l,
-                                     __uint_as_float(o[4 * q + 2]) * inv_l, __uint_as_float(o[4 * q + 3]) * inv_l);
+            for (int hq = 0; hq < 2; ++hq) {  // 16 fp32 columns = 64 bytes at a time
+              uint4 c4[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                c4[q] = make_uint4(__float_as_uint(__uint_as_float(o[16 * hq + 4 * q]) * inv_l),
+                                   __float_as_uint(__uint_as_float(o[16 * hq + 4 * q + 1]) * inv_l),
+                                   __float_as_uint(__uint_as_float(o[16 * hq + 4 * q + 2]) * inv_l),
+                                   __float_as_uint(__uint_as_float(o[16 * hq + 4 * q + 3]) * inv_l));
+              store_rows(c4, [&](int h) {
+                return reinterpret_cast<uint4*>(p.part_o + (((size_t)w * 2 + cd.slot) * p.heads + h) * kDimCkv +
+                                                d0 + 16 * hq);
+              });
             }
           }
         }
