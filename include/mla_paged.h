@@ -87,8 +87,11 @@ typedef struct mla_dims {
  *   sm_scale   softmax scale multiplying the q.k dot product
  *   out        [batch, H, 512] bf16 (written)   lse [batch, H] fp32, natural log (written)
  *   workspace  device scratch of at least mla_workspace_bytes(dims, 0) bytes, caller-owned;
- *              it holds split-KV partial results and the device status word.  Calls that
- *              share a workspace must not overlap on the GPU.
+ *              it holds split-KV partial results, merge counters and the device status
+ *              word.  Zero-fill it before its first use; every call leaves the counters
+ *              at zero again, but after a call that reported a device error (read with
+ *              mla_read_device_status) zero-fill it once more.  Calls that share a
+ *              workspace must not overlap on the GPU.
  *   flags      MLA_VALIDATE or 0;  stream: cudaStream_t
  * Returns MLA_OK or a negative mla_status; nothing is launched on an argument error.
  */

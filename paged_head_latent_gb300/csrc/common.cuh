@@ -37,18 +37,20 @@ struct MlaParams {
   // workspace
   uint32_t* status;         // device status word
   CombineRecord* records;   // [G]
+  int* merge_count;         // [G][ceil(H/8)] chunk-merge arrivals (zero between calls)
   float* part_lse;          // [G][2][H]  base-2 lse of partial fragments
   float* part_o;            // [G][2][H][512] normalised partial outputs
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout: [status (256 B)] [records: G x 16 B] [part_lse] [part_o].
+// Workspace layout: [status (256 B)] [records: G x 20 B] [merge counters] [part_lse] [part_o].
 struct WorkspaceLayout {
-  size_t records, part_lse, part_o, total;
+  size_t records, merge_count, part_lse, part_o, total;
   __host__ __device__ WorkspaceLayout(int G, int H) {
     records = 256;
-    part_lse = align_up(records + (size_t)G * sizeof(CombineRecord), 256);
+    merge_count = align_up(records + (size_t)G * sizeof(CombineRecord), 256);
+    part_lse = align_up(merge_count + (size_t)G * ((H + 7) / 8) * sizeof(int), 256);
     part_o = align_up(part_lse + (size_t)G * 2 * H * sizeof(float), 256);
     total = align_up(part_o + (size_t)G * 2 * H * kDimCkv * sizeof(float), 256);
   }

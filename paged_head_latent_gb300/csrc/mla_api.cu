@@ -233,6 +233,7 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.records = reinterpret_cast<mla::CombineRecord*>(ws + lay.records);
+  p.merge_count = reinterpret_cast<int*>(ws + lay.merge_count);
   p.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   p.part_o = reinterpret_cast<float*>(ws + lay.part_o);
 

@@ -290,7 +290,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int kpe_col = (int)rank * 32;
     TileIter it;
     it.init(pa, cur, T, w, p.workers);
-    if (rank == 0 && lane == 0) p.records[w] = make_record(it.live, it.seg, T, p.workers);
     TileDesc* desc = reinterpret_cast<TileDesc*>(smem + kOffDesc);
     uint32_t j = 0;
     for (; it.live; it.advance(), ++j) {
@@ -386,6 +385,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           mma_commit(bar(S_FULL));
         }
       } else {
+        // This thread idles until the first P exists: write the worker's merge record.
+        if (rank == 0) {
+          TileIter first;
+          first.init(pa, cur, T, w, p.workers);
+          p.records[w] = make_record(first.live, first.seg, T, p.workers);
+        }
         // O += P . V for every tile (TS form: P in TMEM, V = the ckv half of the tile).
         // The tile's descriptor is visible here: the softmax warps read it after the
         // tile's KV_FULL and only then arrive on P_FULL.

@@ -232,22 +232,23 @@ struct Walker {
 
 // Per-worker record read by the combine kernel: the row this worker must merge.
 struct CombineRecord {
-  int row;         // -1: nothing to merge
+  int row;         // row of this worker's first segment if that row is split; else -1
   int w_first;     // first worker holding a fragment of the row
-  int slot_first;  // slot of that worker's fragment
+  int slot_first;  // slot of that worker's fragment (every later worker holds it in slot 0)
+  int w_last;      // last worker holding a fragment of the row (it owns the merge)
   int total_tiles; // T of the call (to skip workers with an empty range)
 };
 
-// Record for worker w given its first segment (or none).
+// Record for worker w given its first segment (or none): which split row the worker's
+// slot-0 fragment belongs to, and the workers that share the row.
 __device__ __forceinline__ CombineRecord make_record(bool has_first, const Segment& s,
                                                      long long T, int G) {
-  CombineRecord rec{-1, 0, 0, (int)T};
-  // A row is merged by the worker holding its last tile.  If this worker's first
-  // segment ends a row that began in an earlier worker, that is this worker.
-  if (has_first && !s.whole && s.t_begin > 0 && s.t_end == row_tiles(s.len)) {
+  CombineRecord rec{-1, 0, 0, 0, (int)T};
+  if (has_first && !s.whole) {
     rec.row = s.row;
     rec.w_first = worker_of(s.row_tile0, T, G);
     rec.slot_first = (worker_start(rec.w_first, T, G) == s.row_tile0) ? 0 : 1;
+    rec.w_last = worker_of(s.row_tile0 + row_tiles(s.len) - 1, T, G);
   }
   return rec;
 }
