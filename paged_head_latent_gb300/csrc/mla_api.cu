@@ -149,17 +149,12 @@ int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uin
 // 64-slot page, or one gathered row), 32-column kpe boxes in 64-byte swizzle (each CTA
 // of a pair takes half of the 64 positional dims), and query rows (L2 prefetch only).
 int build_maps(const MlaParams& p, mla::TmaMaps* m) {
-  const uint64_t qrows = (uint64_t)p.rows * p.heads;
   const uint64_t slots = (uint64_t)p.num_slots;
   const auto sw128 = CU_TENSOR_MAP_SWIZZLE_128B, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
   const auto l256 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B, l128 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   int st;
-  if ((st = get_map(&m->q_nope, p.q_nope, qrows, 512, 64, 128, sw128, l256)) != MLA_OK) return st;
-  if ((st = get_map(&m->q_pe, p.q_pe, qrows, 64, 64, 128, sw128, l128)) != MLA_OK) return st;
   if ((st = get_map(&m->ckv, p.ckv, slots, 512, 64, 64, sw128, l256)) != MLA_OK) return st;
   if ((st = get_map(&m->kpe, p.kpe, slots, 64, 32, 64, sw64, l128)) != MLA_OK) return st;
-  if ((st = get_map(&m->ckv_g, p.ckv, slots, 512, 64, 1, sw128, l256)) != MLA_OK) return st;
-  if ((st = get_map(&m->kpe_g, p.kpe, slots, 64, 32, 1, sw64, l128)) != MLA_OK) return st;
   return MLA_OK;
 }
 

@@ -45,10 +45,11 @@
 //              shared memory and a 64-thread named barrier.  The loop is software
 //              pipelined: tile j+1's partial S leaves for the peer before tile j's
 //              softmax runs, and tile j+2's S is being computed meanwhile.
-//   warp 8     TMA producer: one box load per column chunk when the tile's 64 slots
-//              are contiguous (a whole page of 64), else tile::gather4 row loads; rows
-//              past the row's length read a slot outside the cache, which TMA fills
-//              with zeros.
+//   warp 8     producer: one TMA box load per column chunk when the tile's 64 slots
+//              are contiguous (a whole page of 64); otherwise every lane copies
+//              16-byte pieces of the gathered rows with cp.async into the same
+//              swizzled layout (TMA's row gather was measured slower).  Keys past the
+//              row's length are zero-filled.
 //   warp 9     issues S = Q.K^T (one thread) and owns TMEM
 //   warp 10    issues O += P.V (one thread); tcgen05.mma issue blocks while the tensor
 //              pipe is busy, so the two products get separate issuing threads.
@@ -180,11 +181,11 @@ struct TileDesc {
   int row;       // query row (decode: request)
   int slot;      // partial-result slot of the segment
   int nseg;      // index of the segment among this worker's segments
-  int flags;     // kFirst | kLast | kWhole
+  int flags;     // kFirst | kLast | kWhole | kCopied (loaded by cp.async, not TMA)
   int next_row;  // query row of the next segment when kLast, else -1
   int pad;
 };
-constexpr int kFirst = 1, kLast = 2, kWhole = 4;
+constexpr int kFirst = 1, kLast = 2, kWhole = 4, kCopied = 8;
 static_assert(sizeof(TileDesc) == 32, "descriptor size");
 
 }  // namespace
@@ -260,8 +261,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&maps.ckv);
       prefetch_tensormap(&maps.kpe);
-      prefetch_tensormap(&maps.ckv_g);
-      prefetch_tensormap(&maps.kpe_g);
     }
     // Slot ids of tile t of a segment: lanes hold keys lane and lane + 32; keys past
     // the row's length get a slot outside the cache (TMA reads zeros there).
@@ -275,16 +274,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
                        first <= p.num_slots - kTileKeys;
       contiguous = __all_sync(0xffffffffu, run);
-    };
-    // Rows 4g .. 4g+3 of the tile for lane g < 16.
-    auto gather_rows = [&](int s0, int s1, int (&r)[4]) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int key = 4 * (lane & 15) + q;
-        const int v0 = __shfl_sync(0xffffffffu, s0, key & 31);
-        const int v1 = __shfl_sync(0xffffffffu, s1, key & 31);
-        r[q] = key < 32 ? v0 : v1;
-      }
     };
     const int ckv_col = (int)rank * 256;
     const int kpe_col = (int)rank * 32;
@@ -310,7 +299,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         d.row = it.seg.row;
         d.slot = it.seg.slot;
         d.nseg = it.nseg;
-        d.flags = (it.first() ? kFirst : 0) | (it.last() ? kLast : 0) | (it.seg.whole ? kWhole : 0);
+        d.flags = (it.first() ? kFirst : 0) | (it.last() ? kLast : 0) | (it.seg.whole ? kWhole : 0) |
+                  (contiguous ? 0 : kCopied);
         d.next_row = -1;
         if (it.last()) {
           TileIter peek = it;
@@ -325,8 +315,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         desc[j % kDescRing] = d;
-        if (j == 0) mbar_arrive(bar(DESC0));       // lets the softmax warps load Q early
-        mbar_arrive_expect_tx(kvbar, kStageBytes);  // release: orders the descriptor before the tile
+        if (j == 0) mbar_arrive(bar(DESC0));  // lets the softmax warps load Q early
+        // TMA tile: the one arrival, with the tile's bytes (release: orders the descriptor
+        // before the tile).  Copied tile: lane 0 arrives after the lanes' copies below.
+        if (contiguous) mbar_arrive_expect_tx(kvbar, kStageBytes);
       }
       __syncwarp();
       if (contiguous) {
@@ -335,14 +327,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tma_load_2d(dst + 4 * kChunkKV, &maps.kpe, kpe_col, first, kvbar);
         }
       } else {
-        int r[4];
-        gather_rows(s0, s1, r);
-        if (lane < 16) {
-          for (int c = 0; c < 4; ++c)
-            tma_gather4(dst + c * kChunkKV + lane * 512, &maps.ckv_g, ckv_col + c * 64, r[0], r[1], r[2], r[3],
-                        kvbar);
-          tma_gather4(dst + 4 * kChunkKV + lane * 256, &maps.kpe_g, kpe_col, r[0], r[1], r[2], r[3], kvbar);
+        // Scattered slots: each key's 512-byte ckv half-row is one warp-wide 16-byte
+        // cp.async per lane; the kpe rows go eight keys per instruction.  The shared
+        // addresses follow the 128-byte (ckv) and 64-byte (kpe) swizzles the MMA
+        // descriptors expect.  Keys past the row's length and slots outside the cache
+        // are zero-filled.
+        const char* ckv_src = reinterpret_cast<const char*>(p.ckv + ckv_col) + lane * 16;
+        const uint32_t cu = lane & 7, cc = lane >> 3;
+#pragma unroll 8
+        for (int k = 0; k < kTileKeys; ++k) {
+          const int slot = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
+          const bool okk = slot >= 0 && slot < p.num_slots;
+          cp_async_16_zfill(dst + cc * kChunkKV + k * 128 + ((cu ^ (k & 7)) << 4),
+                            ckv_src + (okk ? (size_t)slot * (kDimCkv * 2) : 0), okk ? 16 : 0);
         }
+        const char* kpe_src = reinterpret_cast<const char*>(p.kpe + kpe_col) + (lane & 3) * 16;
+#pragma unroll
+        for (int i = 0; i < kTileKeys / 8; ++i) {
+          const int k = 8 * i + (lane >> 2);
+          const int slot = __shfl_sync(0xffffffffu, i < 4 ? s0 : s1, k & 31);
+          const bool okk = slot >= 0 && slot < p.num_slots;
+          cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
+                            kpe_src + (okk ? (size_t)slot * (kDimKpe * 2) : 0), okk ? 16 : 0);
+        }
+        cp_async_mbar_arrive(kvbar);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(kvbar);
       }
       __syncwarp();
     }
@@ -374,6 +384,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout)) ||
               (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout)))
             break;
+          if (d.flags & kCopied) fence_proxy_async_smem();  // written through the generic proxy
           tc_fence_after();
           const uint32_t kv = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll
@@ -401,6 +412,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const bool first = d.flags & kFirst;
           if (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout))
             break;
+          if (d.flags & kCopied) fence_proxy_async_smem();  // written through the generic proxy
           tc_fence_after();
           const uint32_t vbase = sbase + kOffKV + stage * kStageBytes;
 #pragma unroll

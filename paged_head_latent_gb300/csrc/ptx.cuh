@@ -120,14 +120,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Four rows r0..r3 (one box column range starting at `col`) into consecutive rows at dst.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int col, int r0, int r1,
-                                            int r2, int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
+// 16-byte global -> shared copy through L2 (cp.async); bytes past `src_bytes` (0 or
+// 16) are zero-filled, so a zero-byte copy reads nothing and writes zeros.
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// The barrier counts one more arrival, which happens when this thread's earlier
+// cp.async copies have landed (net zero on the pending count of the current phase).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // L2 prefetch of `bytes` contiguous bytes (16-byte aligned address, size a multiple of
@@ -137,22 +139,7 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* ptr, uint32_t bytes
                : "memory");
 }
 
-// L2 prefetch of one box / four gathered rows (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-
-__device__ __forceinline__ void tma_prefetch_gather4(const CUtensorMap* map, int col, int r0, int r1, int r2,
-                                                     int r3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile::gather4 [%0, {%1, %2, %3, %4, %5}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-               : "memory");
-}
-
+// Pull a tensor map (kernel parameter) into the descriptor cache.
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -9,12 +9,8 @@ namespace mla {
 
 // 2-D bf16 tensor maps (box = columns x rows).
 struct TmaMaps {
-  CUtensorMap q_nope;  // [rows*H, 512], box 64 x 128, 128-byte swizzle (L2 prefetch of query rows)
-  CUtensorMap q_pe;    // [rows*H, 64],  box 64 x 128, 128-byte swizzle (L2 prefetch)
-  CUtensorMap ckv;     // [slots, 512],  box 64 x 64, 128-byte swizzle (a whole 64-slot page)
-  CUtensorMap kpe;     // [slots, 64],   box 32 x 64, 64-byte swizzle (half of the positional dims)
-  CUtensorMap ckv_g;   // [slots, 512],  box 64 x 1, 128-byte swizzle (tile::gather4 rows)
-  CUtensorMap kpe_g;   // [slots, 64],   box 32 x 1, 64-byte swizzle
+  CUtensorMap ckv;  // [slots, 512], box 64 x 64, 128-byte swizzle (a whole run of 64 slots)
+  CUtensorMap kpe;  // [slots, 64],  box 32 x 64, 64-byte swizzle (half of the positional dims)
 };
 
 cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream);
