@@ -242,6 +242,38 @@ def profile_read():
     return a.value, b.value, n.value
 
 
+def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
+    """Check and marshal the arguments of one decode or prefill call on a
+    ``workloads.Workload`` once, and return a function of no arguments that makes exactly
+    that C-ABI call again (for loops that repeat a call, such as a benchmark's timed
+    region, where the per-call argument checks would otherwise cost host time)."""
+    prefill = w.kind != "decode"
+    run_workload(w, out=out, lse=lse, workspace=workspace, flags=flags, num_workers=num_workers,
+                 stream=stream)  # validates everything once
+    dims = make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
+                     total_q=w.rows if prefill else 0, num_workers=num_workers)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    if prefill:
+        fn = lib().mla_paged_prefill
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.qo_indptr),
+                _ptr(w.kv_indptr), _ptr(w.kv_indices), float(w.sm_scale), _ptr(out), _ptr(lse),
+                ctypes.byref(dims), _ptr(workspace), workspace.numel(), int(flags), sp)
+    else:
+        fn = lib().mla_paged_decode
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.kv_indptr),
+                _ptr(w.kv_indices), float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                _ptr(workspace), workspace.numel(), int(flags), sp)
+    keep = (w, out, lse, workspace, stream, dims)  # keep the tensors and dims alive
+
+    def call():
+        st = fn(*args)
+        if st != 0:
+            raise MlaError(st, "mla_paged_prefill" if prefill else "mla_paged_decode")
+        return keep[1], keep[2]
+
+    return call
+
+
 def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, stream=None):
     """Call decode or prefill on a ``workloads.Workload`` whose tensors are on the GPU."""
     if w.kind == "decode":

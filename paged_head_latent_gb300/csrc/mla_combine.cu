@@ -100,6 +100,9 @@ __device__ __forceinline__ void write_final(const MlaParams& p, const CombineRec
 }
 
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams p) {
+  // Launched as a programmatic dependent of the attention kernel: wait until that grid
+  // has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int w = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombineWarps + warp;
@@ -214,7 +217,20 @@ __global__ void mla_validate_kernel(MlaParams p) {
 }
 
 cudaError_t launch_combine(const MlaParams& p, cudaStream_t stream) {
-  mla_combine_kernel<<<dim3(p.workers, (p.heads + kCombineWarps - 1) / kCombineWarps), kCombineThreads, 0, stream>>>(p);
+  // Programmatic stream serialisation: the launch overlaps the attention kernel's tail;
+  // the kernel's griddepcontrol.wait keeps the data dependency.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.workers, (p.heads + kCombineWarps - 1) / kCombineWarps);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, mla_combine_kernel, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

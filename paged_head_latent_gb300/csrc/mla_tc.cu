@@ -764,6 +764,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
+  // The merge kernel, launched with programmatic stream serialisation, may be
+  // scheduled once every CTA got here; it still waits for this grid's completion
+  // (griddepcontrol.wait) before reading anything this kernel wrote.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   cluster_sync();

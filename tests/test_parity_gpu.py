@@ -132,6 +132,25 @@ def test_decode_dominant_key(lib):
     check_full(lib, w)
 
 
+def test_bound_call_repeats_the_call(lib):
+    """bind_workload's prepared call gives the same bits as the checked call, twice."""
+    require_gpu()
+    w = wl.make_decode([300, 64, 1000], num_qo_heads=128, page_size=64, seed=2306).to("cuda")
+    dims = lib.make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices)
+    ws = torch.zeros(lib.workspace_bytes(dims, False), dtype=torch.uint8, device="cuda")
+    ref_out, ref_lse = lib.run_workload(w, workspace=ws)
+    ref_out, ref_lse = ref_out.clone(), ref_lse.clone()
+    out = torch.empty_like(ref_out)
+    lse = torch.empty_like(ref_lse)
+    stream = torch.cuda.current_stream()
+    call = lib.bind_workload(w, out, lse, ws, stream)
+    for _ in range(2):
+        out.zero_()
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+
+
 # -------------------------------------------------------------- small prefill
 
 @pytest.mark.parametrize("q_lens,prefixes,heads,ps", [
