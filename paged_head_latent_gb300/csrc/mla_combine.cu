@@ -24,12 +24,11 @@ constexpr int kCombineThreads = 32 * kCombineWarps;
 constexpr int kChunk = 8;         // fragments merged by one CTA in the first level
 
 // Fragment f (0-based, worker w_first + f) of a record: its slot index in the workspace,
-// or -1 if that worker has an empty range (possible only when tiles < workers).
-__device__ __forceinline__ long long frag_index(const CombineRecord& rec, int f, int G) {
+// or -1 if that worker has no tiles.  Every worker has tiles when each one's share of
+// the cost units exceeds a row's leading units (min_units > kRowCost).
+__device__ __forceinline__ long long frag_index(const MlaParams& p, const CombineRecord& rec, int f) {
   const int wk = rec.w_first + f;
-  const long long T = rec.total_tiles;
-  // Every worker has at least one tile when T >= G, so the division is needed only below.
-  if (T < G && worker_start(wk + 1, T, G) == worker_start(wk, T, G)) return -1;
+  if (rec.min_units <= kRowCost && !p.records[wk].live) return -1;
   return (long long)wk * 2 + (f == 0 ? rec.slot_first : 0);
 }
 
@@ -38,17 +37,16 @@ __device__ __forceinline__ long long frag_index(const CombineRecord& rec, int f,
 // each load of the warp is one 512-byte row); -inf and zeros if no fragment exists.
 __device__ __forceinline__ float merge_range(const MlaParams& p, const CombineRecord& rec, int f0, int f1,
                                              int h, int lane, float4 (&acc)[4]) {
-  const int G = p.workers;
   float mx = -INFINITY;
   for (int f = f0 + lane; f < f1; f += 32) {
-    const long long fi = frag_index(rec, f, G);
+    const long long fi = frag_index(p, rec, f);
     if (fi >= 0) mx = fmaxf(mx, p.part_lse[fi * p.heads + h]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
   for (int f = f0 + lane; f < f1; f += 32) {
-    const long long fi = frag_index(rec, f, G);
+    const long long fi = frag_index(p, rec, f);
     if (fi >= 0) sum += fast_exp2(p.part_lse[fi * p.heads + h] - mx);
   }
 #pragma unroll
@@ -58,7 +56,7 @@ __device__ __forceinline__ float merge_range(const MlaParams& p, const CombineRe
   if (sum == 0.f) return -INFINITY;
   const float lse2 = mx + fast_log2(sum);
   for (int f = f0; f < f1; ++f) {
-    const long long fi = frag_index(rec, f, G);
+    const long long fi = frag_index(p, rec, f);
     if (fi < 0) continue;
     const size_t frag = (size_t)fi * p.heads + h;
     const float wgt = fast_exp2(p.part_lse[frag] - lse2);
@@ -76,9 +74,9 @@ __device__ __forceinline__ float merge_range(const MlaParams& p, const CombineRe
 }
 
 // First existing fragment in [f0, f1), or -1.
-__device__ __forceinline__ long long first_frag(const CombineRecord& rec, int f0, int f1, int G) {
+__device__ __forceinline__ long long first_frag(const MlaParams& p, const CombineRecord& rec, int f0, int f1) {
   for (int f = f0; f < f1; ++f) {
-    const long long fi = frag_index(rec, f, G);
+    const long long fi = frag_index(p, rec, f);
     if (fi >= 0) return fi;
   }
   return -1;
@@ -108,13 +106,12 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   const int h = blockIdx.y * kCombineWarps + warp;
   const CombineRecord rec = p.records[w];
   if (rec.row < 0) return;
-  const int G = p.workers;
   const int F = rec.w_last - rec.w_first + 1;
   const int fw = w - rec.w_first;
   float4 acc[4];
   // One level when the row has few fragments, or when some workers have no tiles (then
   // a chunk's last worker may have no record; the row has at most T < G fragments).
-  if (F <= kChunk || rec.total_tiles < G) {  // the row's last worker merges all fragments
+  if (F <= kChunk || rec.min_units <= kRowCost) {  // the row's last worker merges all fragments
     if (w != rec.w_last || h >= p.heads) return;
     const float lse2 = merge_range(p, rec, 0, F, h, lane, acc);
     write_final(p, rec, h, lane, acc, lse2);
@@ -124,7 +121,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   const int f0 = chunk * kChunk, f1 = min(f0 + kChunk, F);
   if (fw != f1 - 1) return;  // not the last worker of its chunk
   // Level 1: merge this chunk into its first existing fragment's slot (normalised).
-  const long long dst = first_frag(rec, f0, f1, G);
+  const long long dst = first_frag(p, rec, f0, f1);
   if (h < p.heads && dst >= 0) {
     const float lse2 = merge_range(p, rec, f0, f1, h, lane, acc);
     const size_t frag = (size_t)dst * p.heads + h;
@@ -150,14 +147,14 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   // Level 2: chunk k's result sits in its first existing fragment's slot.
   float mx = -INFINITY;
   for (int k = lane; k < nchunks; k += 32) {
-    const long long fi = first_frag(rec, k * kChunk, min(k * kChunk + kChunk, F), G);
+    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
     if (fi >= 0) mx = fmaxf(mx, __ldcg(p.part_lse + fi * p.heads + h));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   float sum = 0.f;
   for (int k = lane; k < nchunks; k += 32) {
-    const long long fi = first_frag(rec, k * kChunk, min(k * kChunk + kChunk, F), G);
+    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
     if (fi >= 0) sum += fast_exp2(__ldcg(p.part_lse + fi * p.heads + h) - mx);
   }
 #pragma unroll
@@ -166,7 +163,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
 #pragma unroll
   for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int k = 0; k < nchunks; ++k) {
-    const long long fi = first_frag(rec, k * kChunk, min(k * kChunk + kChunk, F), G);
+    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
     if (fi < 0) continue;
     const size_t frag = (size_t)fi * p.heads + h;
     const float wgt = fast_exp2(__ldcg(p.part_lse + frag) - lse2);

@@ -101,7 +101,7 @@ enum Bar : uint32_t {
 struct Misc {
   uint32_t tmem;
   int abort;
-  long long T;
+  long long C;  // cost units of the call (0: no tiles)
   Cursor cur;
 };
 
@@ -148,8 +148,8 @@ struct TileIter {
   int t;
   int nseg;  // index of seg among the worker's segments
   bool live;
-  __device__ void init(const PlanArgs& pa, const Cursor& c, long long T, int w, int G) {
-    walk.init(pa, c, T, w, G);
+  __device__ void init(const PlanArgs& pa, const Cursor& c) {
+    walk.init(pa, c);
     nseg = -1;
     live = walk.next(seg);
     if (live) {
@@ -231,14 +231,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices};
   if (warp == 0) {
     Cursor c;
-    const long long T = warp_plan(pa, w, p.workers, &c);
+    const long long C = warp_plan(pa, w, p.workers, &c);
     if (lane == 0) {
       misc.cur = c;
-      misc.T = T;
+      misc.C = C;
       // Start pulling the first query row into L2 now; the softmax warps read it into
       // TMEM as soon as the first tile's descriptor exists.  (If that row turns out to
       // have no keys, the prefetch was merely useless.)
-      if (T > 0 && c.b < p.batch) {
+      if (c.g < c.g_end && c.b < p.batch) {
         const int row = p.qo_indptr ? __ldg(p.qo_indptr + c.b) + c.i : c.b;
         if (row >= 0 && row < p.rows) {
           if (rank == 0) bulk_prefetch_l2(p.q_nope + (size_t)row * p.heads * kDimCkv, p.heads * kDimCkv * 2);
@@ -253,8 +253,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem = misc.tmem;
-  const long long T = misc.abort ? 0 : misc.T;
-  const Cursor cur = misc.cur;
+  const long long C = misc.C;
+  Cursor cur = misc.cur;
+  if (misc.abort) cur.g_end = cur.g;  // no work
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ TMA producer
@@ -278,7 +279,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int ckv_col = (int)rank * 256;
     const int kpe_col = (int)rank * 32;
     TileIter it;
-    it.init(pa, cur, T, w, p.workers);
+    it.init(pa, cur);
     TileDesc* desc = reinterpret_cast<TileDesc*>(smem + kOffDesc);
     uint32_t j = 0;
     for (; it.live; it.advance(), ++j) {
@@ -374,7 +375,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
       constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
       const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
-      const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
+      const uint32_t ntiles = (uint32_t)(cur.g_end - cur.g);
       if (warp == kMmaWarp) {
         // S = Q . K^T for every tile (TS form: Q slice in TMEM, K tile in shared memory).
         for (uint32_t jq = 0; jq < ntiles; ++jq) {
@@ -399,8 +400,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // This thread idles until the first P exists: write the worker's merge record.
         if (rank == 0) {
           TileIter first;
-          first.init(pa, cur, T, w, p.workers);
-          p.records[w] = make_record(first.live, first.seg, T, p.workers);
+          first.init(pa, cur);
+          p.records[w] = make_record(first.live, first.seg, C, p.workers);
         }
         // O += P . V for every tile (TS form: P in TMEM, V = the ckv half of the tile).
         // The tile's descriptor is visible here: the softmax warps read it after the
@@ -527,7 +528,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     const TileDesc* desc = reinterpret_cast<const TileDesc*>(smem + kOffDesc);
-    const uint32_t ntiles = (uint32_t)(worker_start(w + 1, T, p.workers) - worker_start(w, T, p.workers));
+    const uint32_t ntiles = (uint32_t)(cur.g_end - cur.g);
     bool ok = true;
     uint32_t jf = 0;       // tiles fetched
     uint32_t nxt[24];      // own partial scores of tile jf - 1, rounded and packed
