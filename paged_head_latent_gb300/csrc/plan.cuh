@@ -3,7 +3,7 @@
 // Work is counted in key tiles of kTileKeys keys.  A query row that sees L keys
 // owns ceil(L / kTileKeys) tiles; rows are laid out in order (request by request,
 // query by query) to form one global tile sequence of length T.  Starting a row
-// costs the pair about kRowCost tiles' time (loading its Q, writing its output), so
+// costs the pair several tiles' time (loading its Q, writing its output), so
 // the sequence is split by cost: every non-empty row is preceded by kRowCost cost
 // units, each tile is one unit, C = T + kRowCost * (non-empty rows), and worker w of G
 // (a CTA pair) takes the tiles whose units fall in [floor(w*C/G), floor((w+1)*C/G)).
@@ -23,7 +23,7 @@
 namespace mla {
 
 constexpr int kTileKeys = 64;
-constexpr int kRowCost = 3;  // cost units of starting a row (measured: ~3 tiles' time)
+constexpr int kRowCost = 5;  // cost units of starting a row (tuned on the benchmark batches over 2..8)
 
 // Sum over x = 1..n of ceil(x / 64): the tiles of rows with lengths 1..n.
 __device__ __forceinline__ long long cum_tiles(long long n) {
