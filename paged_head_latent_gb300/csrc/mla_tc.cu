@@ -276,6 +276,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                        first <= p.num_slots - kTileKeys;
       contiguous = __all_sync(0xffffffffu, run);
     };
+    const bool decode = p.qo_indptr == nullptr;
+    const uint64_t kv_policy = l2_policy_evict_first();
     const int ckv_col = (int)rank * 256;
     const int kpe_col = (int)rank * 32;
     TileIter it;
@@ -324,8 +326,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (contiguous) {
         if (lane == 0) {
-          for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kChunkKV, &maps.ckv, ckv_col + c * 64, first, kvbar);
-          tma_load_2d(dst + 4 * kChunkKV, &maps.kpe, kpe_col, first, kvbar);
+          if (decode) {  // each KV byte is read once: evict it first
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d_hint(dst + c * kChunkKV, &maps.ckv, ckv_col + c * 64, first, kvbar, kv_policy);
+            tma_load_2d_hint(dst + 4 * kChunkKV, &maps.kpe, kpe_col, first, kvbar, kv_policy);
+          } else {  // prefill rows of a request share its KV tiles through L2
+            for (int c = 0; c < 4; ++c) tma_load_2d(dst + c * kChunkKV, &maps.ckv, ckv_col + c * 64, first, kvbar);
+            tma_load_2d(dst + 4 * kChunkKV, &maps.kpe, kpe_col, first, kvbar);
+          }
         }
       } else {
         // Scattered slots: each key's 512-byte ckv half-row is one warp-wide 16-byte
@@ -507,7 +515,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Store one 16-column slice (64 bytes per head: 4 chunks per lane in c[]) of this
     // warp's heads through the transpose buffer, so that each store instruction writes
     // 64 contiguous bytes of eight heads.  dst(h) is the slice's address for head h.
-    auto store_rows = [&](const uint4 (&c)[4], auto dst) {
+    const uint64_t keep_policy = l2_policy_evict_last();  // partials are read back by the merge
+    auto store_rows = [&](const uint4 (&c)[4], auto dst, bool keep) {
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(stg + stg_slot(lane, k)), "r"(c[k].x),
@@ -522,7 +531,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                      : "=r"(x.x), "=r"(x.y), "=r"(x.z), "=r"(x.w)
                      : "r"(stg + stg_slot(hh, lane & 3))
                      : "memory");
-        if (row0 + hh < p.heads) dst(row0 + hh)[lane & 3] = x;
+        if (row0 + hh < p.heads) {
+          if (keep) st_global_v4_hint(dst(row0 + hh) + (lane & 3), x, keep_policy);
+          else dst(row0 + hh)[lane & 3] = x;
+        }
       }
       __syncwarp();
     };
@@ -733,7 +745,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             store_rows(c4, [&](int h) {
               return reinterpret_cast<uint4*>(p.out + ((size_t)cd.row * p.heads + h) * kDimCkv + d0);
-            });
+            }, false);
           } else {
 #pragma unroll
             for (int hq = 0; hq < 2; ++hq) {  // 16 fp32 columns = 64 bytes at a time
@@ -747,7 +759,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               store_rows(c4, [&](int h) {
                 return reinterpret_cast<uint4*>(p.part_o + (((size_t)w * 2 + cd.slot) * p.heads + h) * kDimCkv +
                                                 d0 + 16 * hq);
-              });
+              }, true);
             }
           }
         }
