@@ -44,11 +44,13 @@ def load_peaks():
 
 def algorithmic_work(w):
     """Bytes and flops the operator must move / do (per call), per unit:
-    1152 B + 4 B index per visible key; 1152 B q + 1024 B out + 4 B lse per (row, head);
-    2 * (576 + 512) flops per (visible key, head)."""
+    1152 B + 4 B index per cached key of a request (a prefill request's query rows share
+    its keys, so each is read once); 1152 B q + 1024 B out + 4 B lse per (row, head);
+    2 * (576 + 512) flops per (visible key, head), a visible key being a (query row, key)
+    pair that the causal mask keeps."""
     keys = w.visible_keys()
     rows_heads = w.rows * w.num_qo_heads
-    nbytes = keys * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
+    nbytes = sum(w.kv_lens()) * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
     flops = keys * w.num_qo_heads * 2 * (576 + 512)
     return nbytes, flops, keys
 
