@@ -32,42 +32,103 @@ __device__ __forceinline__ long long frag_index(const MlaParams& p, const Combin
   return (long long)wk * 2 + (f == 0 ? rec.slot_first : 0);
 }
 
-// Merge fragments [f0, f1) of a record for head h (one warp).  Returns the base-2 lse
-// and leaves the merged output in acc (lane owns dims 4*lane + 128*q, q = 0..3, so
-// each load of the warp is one 512-byte row); -inf and zeros if no fragment exists.
-__device__ __forceinline__ float merge_range(const MlaParams& p, const CombineRecord& rec, int f0, int f1,
-                                             int h, int lane, float4 (&acc)[4]) {
-  float mx = -INFINITY;
-  for (int f = f0 + lane; f < f1; f += 32) {
-    const long long fi = frag_index(p, rec, f);
-    if (fi >= 0) mx = fmaxf(mx, p.part_lse[fi * p.heads + h]);
+template <bool kCg>
+__device__ __forceinline__ float load_f(const float* ptr) {
+  if constexpr (kCg) return __ldcg(ptr);
+  else return *ptr;
+}
+template <bool kCg>
+__device__ __forceinline__ float4 load_f4(const float4* ptr) {
+  if constexpr (kCg) return __ldcg(ptr);
+  else return *ptr;
+}
+
+// Two positions' rows: lanes k and k + 1 of fi name their slots (-1: none).
+template <bool kCg>
+__device__ __forceinline__ void load_rows(const MlaParams& p, long long fi, int k, int n, int h, int lane,
+                                          float4 (&v)[2][4]) {
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const long long fu = __shfl_sync(0xffffffffu, fi, (k + u) & 31);
+    const bool use = k + u < n && fu >= 0;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + ((size_t)(use ? fu : 0) * p.heads + h) * kDimCkv);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) v[u][q] = use ? load_f4<kCg>(src + lane + 32 * q) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+}
+__device__ __forceinline__ void add_rows(float wgt, int k, const float4 (&v)[2][4], float4 (&acc)[4]) {
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  for (int f = f0 + lane; f < f1; f += 32) {
-    const long long fi = frag_index(p, rec, f);
-    if (fi >= 0) sum += fast_exp2(p.part_lse[fi * p.heads + h] - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (sum == 0.f) return -INFINITY;
-  const float lse2 = mx + fast_log2(sum);
-  for (int f = f0; f < f1; ++f) {
-    const long long fi = frag_index(p, rec, f);
-    if (fi < 0) continue;
-    const size_t frag = (size_t)fi * p.heads + h;
-    const float wgt = fast_exp2(p.part_lse[frag] - lse2);
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + frag * kDimCkv);
+  for (int u = 0; u < 2; ++u) {
+    const float wg = __shfl_sync(0xffffffffu, wgt, (k + u) & 31);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const float4 v = src[lane + 32 * q];
-      acc[q].x = fmaf(wgt, v.x, acc[q].x);
-      acc[q].y = fmaf(wgt, v.y, acc[q].y);
-      acc[q].z = fmaf(wgt, v.z, acc[q].z);
-      acc[q].w = fmaf(wgt, v.w, acc[q].w);
+      acc[q].x = fmaf(wg, v[u][q].x, acc[q].x);
+      acc[q].y = fmaf(wg, v[u][q].y, acc[q].y);
+      acc[q].z = fmaf(wg, v[u][q].z, acc[q].z);
+      acc[q].w = fmaf(wg, v[u][q].w, acc[q].w);
+    }
+  }
+}
+
+// Merge the fragments at positions [f0, f1) for head h (one warp); slot(f) is the
+// workspace slot of position f, or -1 if there is none.  Returns the base-2 lse and
+// leaves the merged output in acc (lane owns dims 4*lane + 128*q, q = 0..3, so each load
+// of the warp is one 512-byte row); -inf and zeros if no fragment exists.  The lanes
+// gather the positions' slots and lse values (32 at a time); the first two rows are
+// loaded while the statistics are reduced, and the rows are accumulated in position
+// order, two loads in flight at a time.  kCg reads through L2 only (data written by
+// other CTAs of this grid).
+template <bool kCg, typename SlotFn>
+__device__ __forceinline__ float merge_range(const MlaParams& p, int f0, int f1, int h, int lane,
+                                             SlotFn slot, float4 (&acc)[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const int n0 = min(32, f1 - f0);
+  const long long fi0 = lane < n0 ? slot(f0 + lane) : -1;
+  const float ls0 = fi0 >= 0 ? load_f<kCg>(p.part_lse + fi0 * p.heads + h) : -INFINITY;
+  float4 v[2][4];
+  load_rows<kCg>(p, fi0, 0, n0, h, lane, v);
+  // Running (max, sum of 2^(lse - max)) of this lane's positions.
+  float mx = -INFINITY, sum = 0.f;
+  for (int b0 = f0; b0 < f1; b0 += 32) {
+    float ls = ls0;
+    if (b0 != f0) {
+      const long long fi = b0 + lane < f1 ? slot(b0 + lane) : -1;
+      ls = fi >= 0 ? load_f<kCg>(p.part_lse + fi * p.heads + h) : -INFINITY;
+    }
+    if (ls > -INFINITY) {  // (a fragment with no weight adds nothing)
+      const float m2 = fmaxf(mx, ls);
+      sum = sum * fast_exp2(mx - m2) + fast_exp2(ls - m2);
+      mx = m2;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, mx, o);
+    const float so = __shfl_xor_sync(0xffffffffu, sum, o);
+    const float m2 = fmaxf(mx, mo);
+    sum = (sum == 0.f ? 0.f : sum * fast_exp2(mx - m2)) + (so == 0.f ? 0.f : so * fast_exp2(mo - m2));
+    mx = m2;
+  }
+  if (sum == 0.f) return -INFINITY;
+  const float lse2 = mx + fast_log2(sum);
+  for (int b0 = f0; b0 < f1; b0 += 32) {
+    const int n = min(32, f1 - b0);
+    long long fi = fi0;
+    float ls = ls0;
+    if (b0 != f0) {
+      fi = lane < n ? slot(b0 + lane) : -1;
+      ls = fi >= 0 ? load_f<kCg>(p.part_lse + fi * p.heads + h) : -INFINITY;
+    }
+    const float wgt = ls > -INFINITY ? fast_exp2(ls - lse2) : 0.f;
+    int k = 0;
+    if (b0 == f0) {  // the two rows loaded above
+      add_rows(wgt, 0, v, acc);
+      k = 2;
+    }
+    for (; k < n; k += 2) {
+      load_rows<kCg>(p, fi, k, n, h, lane, v);
+      add_rows(wgt, k, v, acc);
     }
   }
   return lse2;
@@ -97,6 +158,8 @@ __device__ __forceinline__ void write_final(const MlaParams& p, const CombineRec
   if (lane == 0) p.lse[(size_t)rec.row * p.heads + h] = lse2 * 0.69314718055994531f;
 }
 
+// At most 48 registers: five CTAs per SM, so the whole grid (most of whose CTAs exit at
+// once) is resident in one wave.
 __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams p) {
   // Launched as a programmatic dependent of the attention kernel: wait until that grid
   // has completed and its writes are visible.
@@ -113,7 +176,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   // a chunk's last worker may have no record; the row has at most T < G fragments).
   if (F <= kChunk || rec.min_units <= kRowCost) {  // the row's last worker merges all fragments
     if (w != rec.w_last || h >= p.heads) return;
-    const float lse2 = merge_range(p, rec, 0, F, h, lane, acc);
+    const float lse2 = merge_range<false>(p, 0, F, h, lane, [&](int f) { return frag_index(p, rec, f); }, acc);
     write_final(p, rec, h, lane, acc, lse2);
     return;
   }
@@ -123,7 +186,7 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   // Level 1: merge this chunk into its first existing fragment's slot (normalised).
   const long long dst = first_frag(p, rec, f0, f1);
   if (h < p.heads && dst >= 0) {
-    const float lse2 = merge_range(p, rec, f0, f1, h, lane, acc);
+    const float lse2 = merge_range<false>(p, f0, f1, h, lane, [&](int f) { return frag_index(p, rec, f); }, acc);
     const size_t frag = (size_t)dst * p.heads + h;
     float4* o = reinterpret_cast<float4*>(p.part_o + frag * kDimCkv);
 #pragma unroll
@@ -145,38 +208,9 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   if (h >= p.heads) return;
   __threadfence();
   // Level 2: chunk k's result sits in its first existing fragment's slot.
-  float mx = -INFINITY;
-  for (int k = lane; k < nchunks; k += 32) {
-    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
-    if (fi >= 0) mx = fmaxf(mx, __ldcg(p.part_lse + fi * p.heads + h));
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  float sum = 0.f;
-  for (int k = lane; k < nchunks; k += 32) {
-    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
-    if (fi >= 0) sum += fast_exp2(__ldcg(p.part_lse + fi * p.heads + h) - mx);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  const float lse2 = mx + fast_log2(sum);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int k = 0; k < nchunks; ++k) {
-    const long long fi = first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
-    if (fi < 0) continue;
-    const size_t frag = (size_t)fi * p.heads + h;
-    const float wgt = fast_exp2(__ldcg(p.part_lse + frag) - lse2);
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + frag * kDimCkv);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float4 v = __ldcg(src + lane + 32 * q);
-      acc[q].x = fmaf(wgt, v.x, acc[q].x);
-      acc[q].y = fmaf(wgt, v.y, acc[q].y);
-      acc[q].z = fmaf(wgt, v.z, acc[q].z);
-      acc[q].w = fmaf(wgt, v.w, acc[q].w);
-    }
-  }
+  const float lse2 = merge_range<true>(p, 0, nchunks, h, lane, [&](int k) {
+    return first_frag(p, rec, k * kChunk, min(k * kChunk + kChunk, F));
+  }, acc);
   write_final(p, rec, h, lane, acc, lse2);
 }
 
