@@ -243,7 +243,7 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
     mla::TmaMaps maps;
     st = build_maps(p, &maps);
     if (st != MLA_OK) return st;
-    if (mla::launch_tc(maps, p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+    if (mla::launch_tc(maps, p, dims->page_size % 64 != 0, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
   }
   if (ev) cudaEventRecord(ev[1], stream);
   if (mla::launch_combine(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;

@@ -190,6 +190,9 @@ static_assert(sizeof(TileDesc) == 32, "descriptor size");
 
 }  // namespace
 
+// kGather: the cache's pages are smaller than a tile (page size not a multiple of 64),
+// so tiles are copied slot by slot and the producer reads slot ids a tile ahead.
+template <bool kGather>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -264,17 +267,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&maps.kpe);
     }
     // Slot ids of tile t of a segment: lanes hold keys lane and lane + 32; keys past
-    // the row's length get a slot outside the cache (TMA reads zeros there).
+    // the row's length get a slot outside the cache (TMA reads zeros there).  A TMA tile
+    // takes a few instructions, so its ids are loaded just before the wait for its stage;
+    // with small pages (kGather) a copied tile's copies take long to issue, so the next
+    // tile's ids (same row) are loaded before them and are ready when that tile comes up.
+    auto eval_slots = [&](int nvalid, int s0, int s1, bool& contiguous, int& first) {
+      first = __shfl_sync(0xffffffffu, s0, 0);
+      const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
+                       first <= p.num_slots - kTileKeys;
+      contiguous = __all_sync(0xffffffffu, run);
+    };
     auto tile_slots = [&](const Segment& sg, int t, int& s0, int& s1, bool& contiguous, int& first) {
       const int key0 = t * kTileKeys;
       const int nvalid = min(kTileKeys, sg.len - key0);
       const int* ip = p.kv_indices + sg.kv0 + key0;
       s0 = lane < nvalid ? __ldg(ip + lane) : p.num_slots;
       s1 = lane + 32 < nvalid ? __ldg(ip + lane + 32) : p.num_slots;
-      first = __shfl_sync(0xffffffffu, s0, 0);
-      const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
-                       first <= p.num_slots - kTileKeys;
-      contiguous = __all_sync(0xffffffffu, run);
+      eval_slots(nvalid, s0, s1, contiguous, first);
     };
     const bool decode = p.qo_indptr == nullptr;
     const uint64_t kv_policy = l2_policy_evict_first();
@@ -284,12 +293,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     it.init(pa, cur);
     TileDesc* desc = reinterpret_cast<TileDesc*>(smem + kOffDesc);
     uint32_t j = 0;
+    bool have_next = false;  // next_s0/next_s1 hold this tile's ids, loaded a tile ago
+    int next_s0 = 0, next_s1 = 0;
     for (; it.live; it.advance(), ++j) {
       const int stage = j % kStages;
       int s0, s1, first;
       bool contiguous;
-      // Slot ids first, so their load overlaps the wait for a free stage.
-      tile_slots(it.seg, it.t, s0, s1, contiguous, first);
+      if (kGather && have_next) {
+        s0 = next_s0;
+        s1 = next_s1;
+        eval_slots(min(kTileKeys, it.seg.len - it.t * kTileKeys), s0, s1, contiguous, first);
+        have_next = false;
+      } else {
+        // Slot ids first, so their load overlaps the wait for a free stage.
+        tile_slots(it.seg, it.t, s0, s1, contiguous, first);
+      }
       if (j >= kStages &&
           !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout))
         break;
@@ -341,6 +359,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // addresses follow the 128-byte (ckv) and 64-byte (kpe) swizzles the MMA
         // descriptors expect.  Keys past the row's length and slots outside the cache
         // are zero-filled.
+        if (kGather && !it.last()) {  // the next tile of this row
+          const int key1 = (it.t + 1) * kTileKeys;
+          const int nv1 = min(kTileKeys, it.seg.len - key1);
+          const int* ip1 = p.kv_indices + it.seg.kv0 + key1;
+          next_s0 = lane < nv1 ? __ldg(ip1 + lane) : p.num_slots;
+          next_s1 = lane + 32 < nv1 ? __ldg(ip1 + lane + 32) : p.num_slots;
+          have_next = true;
+        }
         const char* ckv_src = reinterpret_cast<const char*>(p.ckv + ckv_col) + lane * 16;
         const uint32_t cu = lane & 7, cc = lane >> 3;
 #pragma unroll 8
@@ -792,16 +818,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 uint32_t tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream) {
-  static bool configured[64] = {};
+cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cudaStream_t stream) {
+  static bool configured[64][2] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (dev >= 0 && dev < 64 && !configured[dev][gather]) {
+    cudaError_t e = gather ? cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)kSmemBytes)
+                           : cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                  (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev] = true;
+    configured[dev][gather] = true;
   }
-  mla_tc_kernel<<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
+  if (gather) mla_tc_kernel<true><<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
+  else mla_tc_kernel<false><<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
 

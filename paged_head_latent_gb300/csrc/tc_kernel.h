@@ -13,7 +13,8 @@ struct TmaMaps {
   CUtensorMap kpe;  // [slots, 64],  box 32 x 64, 64-byte swizzle (half of the positional dims)
 };
 
-cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream);
+// gather: the cache's page size is not a multiple of 64 (tiles are copied slot by slot).
+cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cudaStream_t stream);
 uint32_t tc_smem_bytes();
 
 }  // namespace mla
