@@ -69,6 +69,10 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;    // issues S = Q.K^T; owns TMEM
 constexpr int kPvWarp = 10;    // issues O += P.V
 constexpr int kThreads = 352;
+// The small-page instance has a second copy warp: a copied tile's keys are split
+// between the two warps (32 each).
+constexpr int kCopyWarp2 = 11;
+constexpr int kThreadsGather = 384;
 constexpr int kStages = 4;
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
@@ -193,7 +197,7 @@ static_assert(sizeof(TileDesc) == 32, "descriptor size");
 // kGather: the cache's pages are smaller than a tile (page size not a multiple of 64),
 // so tiles are copied slot by slot and the producer reads slot ids a tile ahead.
 template <bool kGather>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGather : kThreads, 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -211,7 +215,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (misc.abort) atomicOr(p.status, kStatusTimeout);
     mbar_init(bar(Q_FULL), kSoftmaxWarps);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(bar(KV_FULL0 + s), 1);
+      mbar_init(bar(KV_FULL0 + s), kGather ? 2 : 1);  // one arrival per copy warp
       mbar_init(bar(KV_EMPTY0 + s), 1);
     }
     mbar_init(bar(S_FULL), 1);
@@ -260,7 +264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   Cursor cur = misc.cur;
   if (misc.abort) cur.g_end = cur.g;  // no work
 
-  if (warp == kProducerWarp) {
+  if (warp == kProducerWarp || (kGather && warp == kCopyWarp2)) {
+    const int part = kGather && warp == kCopyWarp2 ? 1 : 0;  // copy warp index
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       prefetch_tensormap(&maps.ckv);
@@ -313,7 +318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       const uint32_t kvbar = bar(KV_FULL0 + stage);
       const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
-      if (lane == 0) {
+      if (lane == 0 && part == 0) {
         TileDesc d;
         d.t = it.t;
         d.len = it.seg.len;
@@ -343,7 +348,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (contiguous) {
-        if (lane == 0) {
+        if (kGather && part == 1) {
+          if (lane == 0) mbar_arrive(kvbar);
+        } else if (lane == 0) {
           if (decode) {  // each KV byte is read once: evict it first
             for (int c = 0; c < 4; ++c)
               tma_load_2d_hint(dst + c * kChunkKV, &maps.ckv, ckv_col + c * 64, first, kvbar, kv_policy);
@@ -369,21 +376,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const char* ckv_src = reinterpret_cast<const char*>(p.ckv + ckv_col) + lane * 16;
         const uint32_t cu = lane & 7, cc = lane >> 3;
-#pragma unroll 8
-        for (int k = 0; k < kTileKeys; ++k) {
-          const int slot = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
-          const bool okk = slot >= 0 && slot < p.num_slots;
-          cp_async_16_zfill(dst + cc * kChunkKV + k * 128 + ((cu ^ (k & 7)) << 4),
-                            ckv_src + (okk ? (size_t)slot * (kDimCkv * 2) : 0), okk ? 16 : 0);
-        }
         const char* kpe_src = reinterpret_cast<const char*>(p.kpe + kpe_col) + (lane & 3) * 16;
+        if constexpr (kGather) {  // this warp's 32 keys: part * 32 .. + 31
+          const int sp = part ? s1 : s0;
+#pragma unroll 8
+          for (int kk = 0; kk < 32; ++kk) {
+            const int k = 32 * part + kk;
+            const int slot = __shfl_sync(0xffffffffu, sp, kk);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(dst + cc * kChunkKV + k * 128 + ((cu ^ (k & 7)) << 4),
+                              ckv_src + (okk ? (size_t)slot * (kDimCkv * 2) : 0), okk ? 16 : 0);
+          }
 #pragma unroll
-        for (int i = 0; i < kTileKeys / 8; ++i) {
-          const int k = 8 * i + (lane >> 2);
-          const int slot = __shfl_sync(0xffffffffu, i < 4 ? s0 : s1, k & 31);
-          const bool okk = slot >= 0 && slot < p.num_slots;
-          cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
-                            kpe_src + (okk ? (size_t)slot * (kDimKpe * 2) : 0), okk ? 16 : 0);
+          for (int i = 0; i < 4; ++i) {
+            const int kk = 8 * i + (lane >> 2), k = 32 * part + kk;
+            const int slot = __shfl_sync(0xffffffffu, sp, kk);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
+                              kpe_src + (okk ? (size_t)slot * (kDimKpe * 2) : 0), okk ? 16 : 0);
+          }
+        } else {
+#pragma unroll 8
+          for (int k = 0; k < kTileKeys; ++k) {
+            const int slot = __shfl_sync(0xffffffffu, k < 32 ? s0 : s1, k & 31);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(dst + cc * kChunkKV + k * 128 + ((cu ^ (k & 7)) << 4),
+                              ckv_src + (okk ? (size_t)slot * (kDimCkv * 2) : 0), okk ? 16 : 0);
+          }
+#pragma unroll
+          for (int i = 0; i < kTileKeys / 8; ++i) {
+            const int k = 8 * i + (lane >> 2);
+            const int slot = __shfl_sync(0xffffffffu, i < 4 ? s0 : s1, k & 31);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
+                              kpe_src + (okk ? (size_t)slot * (kDimKpe * 2) : 0), okk ? 16 : 0);
+          }
         }
         cp_async_mbar_arrive(kvbar);
         __syncwarp();
@@ -830,7 +857,7 @@ cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cuda
     if (e != cudaSuccess) return e;
     configured[dev][gather] = true;
   }
-  if (gather) mla_tc_kernel<true><<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
+  if (gather) mla_tc_kernel<true><<<2 * p.workers, kThreadsGather, kSmemBytes, stream>>>(maps, p);
   else mla_tc_kernel<false><<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
