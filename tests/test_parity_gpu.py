@@ -70,6 +70,22 @@ def test_decode_page_layouts(lib, page_size, shuffle):
     check_full(lib, w)
 
 
+@pytest.mark.parametrize("layout", ["sequential", "mixed"])
+def test_decode_small_pages_with_runs(lib, layout):
+    """Page size 1 (the small-page kernel instance, two copy warps) whose slots form runs
+    of 64: such tiles come in as TMA boxes, the others are copied.  "sequential" makes
+    every full tile a run; "mixed" reverses every other tile's slots so runs and copies
+    alternate within each request."""
+    w = wl.make_decode([700, 129, 64, 300, 5], num_qo_heads=128, page_size=1, seed=2110)
+    n = w.num_kv_indices
+    idx = torch.arange(n, dtype=torch.int32)
+    if layout == "mixed":
+        for t0 in range(64, n, 128):  # reverse the slots of every other 64-entry block
+            idx[t0:t0 + 64] = idx[t0:t0 + 64].flip(0)
+    w = dataclasses.replace(w, kv_indices=idx)
+    check_full(lib, w)
+
+
 def test_decode_empty_request(lib):
     w = wl.make_decode([0, 5, 0, 130], num_qo_heads=32, page_size=16, seed=2201)
     check_full(lib, w)
