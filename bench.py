@@ -238,9 +238,7 @@ def our_arm(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
     with torch.cuda.stream(stream):
-        dims = mla.make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
-                             total_q=w.rows if w.kind == "prefill" else 0)
-        ws = torch.zeros(mla.workspace_bytes(dims, w.kind == "prefill"), dtype=torch.uint8, device=dev)
+        ws = torch.zeros(mla.workload_workspace_bytes(w), dtype=torch.uint8, device=dev)
         # The C-ABI call with its arguments checked and marshalled once.
         call = mla.bind_workload(w, out, lse, ws, stream)
         for _ in range(max(args.warmup, 3)):

@@ -116,6 +116,27 @@ int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cach
                       void* stream);
 
 /*
+ * Packed multi-token decode (speculative / MTP decode): every request has the same
+ * number q_len >= 1 of new query tokens, causal within the request: token i of request
+ * b sees the first kv_len_b - q_len + i + 1 of its keys (kv_len_b >= q_len is required;
+ * MLA_VALIDATE flags shorter requests).  This is the fixed-Q form of the packed-query
+ * decode in flashinfer's prims_ts wrapper (batch_mla_decode_with_paged_kv_cache,
+ * parameters qo_indptr / max_seq_len_q, mask_type "causal"), and FlashMLA's
+ * flash_mla_with_kvcache with seq_len_q > 1: the q_len tokens of a request share each
+ * KV tile, q_len * H rows per tile.
+ *   q_nope [batch, q_len, H, 512], q_pe [batch, q_len, H, 64] bf16
+ *   out    [batch, q_len, H, 512] bf16, lse [batch, q_len, H] fp32 (natural log)
+ *   q_len * num_qo_heads must be <= 128 (else MLA_ERR_DIMS; use mla_paged_prefill with
+ *   qo_indptr for more rows per request).
+ *   workspace >= mla_workspace_bytes_mtp(dims, q_len); other arguments as for
+ *   mla_paged_decode (dims->total_q is ignored).
+ */
+int mla_paged_decode_mtp(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                         const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                         float sm_scale, void* out, float* lse, const mla_dims* dims, int q_len,
+                         void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
  * Paged MLA decode for callers that cannot allocate device memory (a plugin that runs
  * inside another framework's memory pool, code that must not call cudaMalloc after
  * start-up, or a context where an allocation would synchronise the device).  This entry
@@ -140,6 +161,10 @@ int mla_paged_decode_noalloc(const void* q_nope, const void* q_pe, const void* c
 /* Workspace bytes a call with these dims needs (0 on invalid dims).  With
  * dims->num_workers == 0 it queries the current device's SM count. */
 size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill);
+
+/* Workspace bytes of mla_paged_decode_mtp with q_len tokens per request (0 on invalid
+ * dims or q_len * num_qo_heads > 128). */
+size_t mla_workspace_bytes_mtp(const mla_dims* dims, int q_len);
 
 /* Number of split-KV workers (CTA pairs) used when dims->num_workers == 0, for the
  * current device; negative mla_status on failure. */

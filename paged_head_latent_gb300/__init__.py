@@ -49,9 +49,13 @@ _SIGNATURES = [
     ("mla_paged_prefill", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
       ctypes.c_int, _P]),
+    ("mla_paged_decode_mtp", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P,
+      ctypes.c_size_t, ctypes.c_int, _P]),
     ("mla_paged_decode_noalloc", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P]),
     ("mla_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
+    ("mla_workspace_bytes_mtp", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
     ("mla_default_num_workers", ctypes.c_int, []),
     ("mla_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("mla_read_device_status", ctypes.c_int, [_P, _P]),
@@ -95,6 +99,24 @@ def make_dims(batch, num_qo_heads, num_pages, page_size, num_kv_indices, total_q
 
 def workspace_bytes(dims: MlaDims, is_prefill: bool) -> int:
     return int(lib().mla_workspace_bytes(ctypes.byref(dims), 1 if is_prefill else 0))
+
+
+def workspace_bytes_mtp(dims: MlaDims, q_len: int) -> int:
+    return int(lib().mla_workspace_bytes_mtp(ctypes.byref(dims), int(q_len)))
+
+
+def workload_dims(w, num_workers=0) -> MlaDims:
+    """The dims of a call on a ``workloads.Workload`` (decode, prefill or mtp)."""
+    return make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
+                     total_q=w.rows if w.kind == "prefill" else 0, num_workers=num_workers)
+
+
+def workload_workspace_bytes(w, num_workers=0) -> int:
+    """Workspace bytes a call on ``w`` needs."""
+    dims = workload_dims(w, num_workers)
+    if w.kind == "mtp":
+        return workspace_bytes_mtp(dims, w.mtp_q_len)
+    return workspace_bytes(dims, w.kind == "prefill")
 
 
 def default_num_workers() -> int:
@@ -194,6 +216,51 @@ def mla_paged_prefill(q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, 
                  out, lse, workspace, flags, num_workers, stream)
 
 
+def mla_paged_decode_mtp(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale,
+                         out=None, lse=None, workspace=None, flags=0, num_workers=0,
+                         stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Packed multi-token decode: q_nope [batch, q_len, H, 512], q_pe [batch, q_len, H, 64];
+    token i of a request sees its first kv_len - q_len + i + 1 keys.  Returns (out
+    [batch, q_len, H, 512], lse [batch, q_len, H]).  q_len * H must be <= 128."""
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache), ("kpe_cache", kpe_cache)):
+        _check_cuda(n, t, torch.bfloat16)
+    for n, t in (("kv_indptr", kv_indptr), ("kv_indices", kv_indices)):
+        _check_cuda(n, t, torch.int32)
+    if q_nope.dim() != 4 or q_nope.shape[-1] != HEAD_DIM_CKV:
+        raise ValueError("q_nope must be [batch, q_len, H, 512]")
+    batch, q_len, heads = q_nope.shape[0], q_nope.shape[1], q_nope.shape[2]
+    if q_pe.shape != (batch, q_len, heads, HEAD_DIM_KPE):
+        raise ValueError("q_pe must be [batch, q_len, H, 64]")
+    if kv_indptr.numel() - 1 != batch:
+        raise ValueError("kv_indptr must have batch + 1 entries")
+    num_pages, page_size = _cache_geometry(ckv_cache, kpe_cache)
+    dims = make_dims(batch, heads, num_pages, page_size, kv_indices.numel(), num_workers=num_workers)
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty(batch, q_len, heads, HEAD_DIM_CKV, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(batch, q_len, heads, dtype=torch.float32, device=dev)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("lse", lse, torch.float32)
+    if out.shape != (batch, q_len, heads, HEAD_DIM_CKV) or lse.shape != (batch, q_len, heads):
+        raise ValueError("out must be [batch, q_len, H, 512] and lse [batch, q_len, H]")
+    need = workspace_bytes_mtp(dims, q_len)
+    if need == 0:
+        raise MlaError(-2, "mla_workspace_bytes_mtp")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = lib().mla_paged_decode_mtp(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                        _ptr(kv_indptr), _ptr(kv_indices), float(sm_scale), _ptr(out),
+                                        _ptr(lse), ctypes.byref(dims), int(q_len), _ptr(workspace),
+                                        workspace.numel(), int(flags), ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise MlaError(st, "mla_paged_decode_mtp")
+    return out, lse
+
+
 def mla_paged_decode_noalloc(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale,
                              out, lse, num_workers=0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Paged MLA decode without a workspace argument, for callers that cannot allocate
@@ -247,13 +314,18 @@ def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
     ``workloads.Workload`` once, and return a function of no arguments that makes exactly
     that C-ABI call again (for loops that repeat a call, such as a benchmark's timed
     region, where the per-call argument checks would otherwise cost host time)."""
-    prefill = w.kind != "decode"
+    prefill = w.kind == "prefill"
     run_workload(w, out=out, lse=lse, workspace=workspace, flags=flags, num_workers=num_workers,
                  stream=stream)  # validates everything once
-    dims = make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
-                     total_q=w.rows if prefill else 0, num_workers=num_workers)
+    dims = workload_dims(w, num_workers)
     sp = ctypes.c_void_p(stream.cuda_stream)
-    if prefill:
+    name = {"decode": "mla_paged_decode", "prefill": "mla_paged_prefill", "mtp": "mla_paged_decode_mtp"}[w.kind]
+    if w.kind == "mtp":
+        fn = lib().mla_paged_decode_mtp
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.kv_indptr),
+                _ptr(w.kv_indices), float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                int(w.mtp_q_len), _ptr(workspace), workspace.numel(), int(flags), sp)
+    elif prefill:
         fn = lib().mla_paged_prefill
         args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.qo_indptr),
                 _ptr(w.kv_indptr), _ptr(w.kv_indices), float(w.sm_scale), _ptr(out), _ptr(lse),
@@ -268,14 +340,23 @@ def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
     def call():
         st = fn(*args)
         if st != 0:
-            raise MlaError(st, "mla_paged_prefill" if prefill else "mla_paged_decode")
+            raise MlaError(st, name)
         return keep[1], keep[2]
 
     return call
 
 
 def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, stream=None):
-    """Call decode or prefill on a ``workloads.Workload`` whose tensors are on the GPU."""
+    """Call decode, prefill or packed multi-token decode on a ``workloads.Workload`` whose
+    tensors are on the GPU.  Returns (out, lse) shaped [rows, H, 512] and [rows, H]."""
+    if w.kind == "mtp":
+        b, q, h = w.batch, w.mtp_q_len, w.num_qo_heads
+        o4 = None if out is None else out.view(b, q, h, HEAD_DIM_CKV)
+        l3 = None if lse is None else lse.view(b, q, h)
+        o4, l3 = mla_paged_decode_mtp(w.q_nope.view(b, q, h, HEAD_DIM_CKV), w.q_pe.view(b, q, h, HEAD_DIM_KPE),
+                                      w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
+                                      o4, l3, workspace, flags, num_workers, stream)
+        return o4.view(b * q, h, HEAD_DIM_CKV), l3.view(b * q, h)
     if w.kind == "decode":
         return mla_paged_decode(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices,
                                 w.sm_scale, out, lse, workspace, flags, num_workers, stream)

@@ -40,6 +40,11 @@ struct MlaParams {
   int* merge_count;         // [G][ceil(H/8)] chunk-merge arrivals (zero between calls)
   float* part_lse;          // [G][2][H]  base-2 lse of partial fragments
   float* part_o;            // [G][2][H][512] normalised partial outputs
+  // Packed multi-token decode (0 otherwise): each request has mtp_q query tokens of
+  // mtp_h heads packed into heads = mtp_q * mtp_h rows; token i sees the first
+  // kv_len - mtp_q + i + 1 keys (causal within the request).
+  int mtp_q;
+  int mtp_h;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -179,12 +179,18 @@ cudaEvent_t* profile_slot() {
   return slot;
 }
 
-int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cache,
+// Rows (query heads) one work row of the kernel holds: H, or q_len * H for packed
+// multi-token decode (q_len > 0).
+int packed_heads(const mla_dims* d, int q_len) { return q_len > 0 ? q_len * d->num_qo_heads : d->num_qo_heads; }
+
+int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const void* ckv_cache,
         const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
         void* workspace, size_t workspace_bytes, int flags, void* stream_ptr) {
   int st = check_dims(dims, prefill);
   if (st != MLA_OK) return st;
+  if (q_len < 0 || packed_heads(dims, q_len) > mla::kMaxHeads) return MLA_ERR_DIMS;
+  if ((long long)dims->batch * packed_heads(dims, q_len) >= (1LL << 31)) return MLA_ERR_DIMS;
   const long long rows = prefill ? dims->total_q : dims->batch;
   if (!q_nope || !q_pe || !kv_indptr || !out || !lse) return MLA_ERR_NULL;
   // The caches may be NULL only when they hold no slot at all.
@@ -198,7 +204,7 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   int G = 0;
   st = resolve_workers(dims, &G);
   if (st != MLA_OK) return st;
-  const mla::WorkspaceLayout lay(G, dims->num_qo_heads);
+  const mla::WorkspaceLayout lay(G, packed_heads(dims, q_len));
   if (!workspace || workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
   if (!aligned16(workspace)) return MLA_ERR_ALIGN;
   if (rows == 0) return MLA_OK;
@@ -218,7 +224,9 @@ int run(bool prefill, const void* q_nope, const void* q_pe, const void* ckv_cach
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
   p.batch = dims->batch;
-  p.heads = dims->num_qo_heads;
+  p.heads = packed_heads(dims, q_len);
+  p.mtp_q = q_len;
+  p.mtp_h = dims->num_qo_heads;
   p.rows = (int)rows;
   p.num_slots = dims->num_pages * dims->page_size;
   // With an empty cache no key can be loaded: treat every request as empty.
@@ -259,7 +267,16 @@ int mla_paged_decode(const void* q_nope, const void* q_pe, const void* ckv_cache
                      const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
                      float sm_scale, void* out, float* lse, const mla_dims* dims,
                      void* workspace, size_t workspace_bytes, int flags, void* stream) {
-  return run(false, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, kv_indptr, kv_indices, sm_scale,
+  return run(false, 0, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, kv_indptr, kv_indices, sm_scale,
+             out, lse, dims, workspace, workspace_bytes, flags, stream);
+}
+
+int mla_paged_decode_mtp(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                         const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
+                         float sm_scale, void* out, float* lse, const mla_dims* dims, int q_len,
+                         void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  if (q_len < 1) return MLA_ERR_DIMS;
+  return run(false, q_len, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, kv_indptr, kv_indices, sm_scale,
              out, lse, dims, workspace, workspace_bytes, flags, stream);
 }
 
@@ -268,7 +285,7 @@ int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cach
                       const int32_t* kv_indices, float sm_scale, void* out, float* lse,
                       const mla_dims* dims, void* workspace, size_t workspace_bytes, int flags,
                       void* stream) {
-  return run(true, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
+  return run(true, 0, q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_indices, sm_scale,
              out, lse, dims, workspace, workspace_bytes, flags, stream);
 }
 
@@ -277,6 +294,13 @@ size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill) {
   int G = 0;
   if (resolve_workers(dims, &G) != MLA_OK) return 0;
   return mla::WorkspaceLayout(G, dims->num_qo_heads).total;
+}
+
+size_t mla_workspace_bytes_mtp(const mla_dims* dims, int q_len) {
+  if (check_dims(dims, false) != MLA_OK || q_len < 1 || packed_heads(dims, q_len) > mla::kMaxHeads) return 0;
+  int G = 0;
+  if (resolve_workers(dims, &G) != MLA_OK) return 0;
+  return mla::WorkspaceLayout(G, packed_heads(dims, q_len)).total;
 }
 
 int mla_default_num_workers(void) {

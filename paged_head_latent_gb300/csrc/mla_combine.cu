@@ -233,6 +233,7 @@ __global__ void mla_validate_kernel(MlaParams p) {
         const int q0 = p.qo_indptr[b], q1 = p.qo_indptr[b + 1];
         if (q1 < q0 || (k1 - k) < (q1 - q0)) bad = true;
       }
+      if (p.mtp_q > 0 && (k1 - k) < p.mtp_q) bad = true;  // packed tokens need kv_len >= q_len
     }
     if (p.qo_indptr) {
       const int q = p.qo_indptr[b];

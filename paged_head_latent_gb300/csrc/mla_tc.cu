@@ -196,7 +196,9 @@ static_assert(sizeof(TileDesc) == 32, "descriptor size");
 
 // kGather: the cache's pages are smaller than a tile (page size not a multiple of 64),
 // so tiles are copied slot by slot and the producer reads slot ids a tile ahead.
-template <bool kGather>
+// kPack: packed multi-token decode; TMEM lane m holds token m / mtp_h, head m % mtp_h of
+// the request, and each token's causal horizon masks the scores lane by lane.
+template <bool kGather, bool kPack>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGather : kThreads, 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -652,6 +654,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
     }
     float m_ref = -INFINITY, l = 0.f;  // l: this thread's 32 columns only
+    // Packed tokens: this lane's token sees lag fewer keys than the request's last one.
+    const int lag = kPack ? p.mtp_q - 1 - row / p.mtp_h : 0;
     uint32_t j = 0;
     while (ok && j < jf) {
       const TileDesc cd = desc[j % kDescRing];  // tile j (KV_FULL seen in fetch)
@@ -693,7 +697,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
           q_pending = -1;
         }
       }
-      const int nvalid = min(kTileKeys, cd.len - cd.t * kTileKeys) - 32 * half;
+      const int nvalid = min(kTileKeys, (kPack ? cd.len - lag : cd.len) - cd.t * kTileKeys) - 32 * half;
       // All 32 keys valid and a non-negative scale (the usual case): the maximum of the
       // scaled scores is the scaled maximum, and the scale folds into the exponent below.
       const bool full = nvalid >= 32 && scale >= 0.f;
@@ -725,11 +729,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
       uint32_t pk[16];
       float sum = 0.f;
+      // A packed token can see no key of a split segment (m_ref = -inf): its P is zero.
+      const float mref = (kPack && m_ref == -INFINITY) ? 0.f : m_ref;
       if (full) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float a = fast_exp2(fmaf(s[2 * k], scale, -m_ref));
-          const float bb = fast_exp2(fmaf(s[2 * k + 1], scale, -m_ref));
+          const float a = fast_exp2(fmaf(s[2 * k], scale, -mref));
+          const float bb = fast_exp2(fmaf(s[2 * k + 1], scale, -mref));
           sum += a + bb;
           __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
           pk[k] = *reinterpret_cast<uint32_t*>(&h);
@@ -737,8 +743,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       } else {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float a = fast_exp2(s[2 * k] - m_ref);
-          const float bb = fast_exp2(s[2 * k + 1] - m_ref);
+          const float a = fast_exp2(s[2 * k] - mref);
+          const float bb = fast_exp2(s[2 * k + 1] - mref);
           sum += a + bb;
           __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
           pk[k] = *reinterpret_cast<uint32_t*>(&h);
@@ -773,7 +779,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         const float lt = l + lbuf[(half ^ 1) * 128 + row];
         if (!mbar_wait(bar(O_FULL), cd.nseg & 1, abort, p.status, kStatusTimeout)) break;
         tc_fence_after();
-        const float inv_l = 1.f / lt;
+        const float inv_l = (kPack && !(lt > 0.f)) ? 0.f : 1.f / lt;  // (no key: out 0, lse -inf)
         const float lse2 = m_ref + fast_log2(lt);
         const bool valid = row < p.heads;
         const size_t frag = ((size_t)w * 2 + cd.slot) * p.heads + row;
@@ -845,21 +851,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
 
 uint32_t tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cudaStream_t stream) {
-  static bool configured[64][2] = {};
+namespace {
+template <bool kGather, bool kPack>
+cudaError_t launch_instance(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream) {
+  static bool configured[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev][gather]) {
-    cudaError_t e = gather ? cudaFuncSetAttribute(mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  (int)kSmemBytes)
-                           : cudaFuncSetAttribute(mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  (int)kSmemBytes);
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<kGather, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    configured[dev][gather] = true;
+    configured[dev] = true;
   }
-  if (gather) mla_tc_kernel<true><<<2 * p.workers, kThreadsGather, kSmemBytes, stream>>>(maps, p);
-  else mla_tc_kernel<false><<<2 * p.workers, kThreads, kSmemBytes, stream>>>(maps, p);
+  mla_tc_kernel<kGather, kPack><<<2 * p.workers, kGather ? kThreadsGather : kThreads, kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cudaStream_t stream) {
+  const bool pack = p.mtp_q > 0;
+  if (gather) return pack ? launch_instance<true, true>(maps, p, stream) : launch_instance<true, false>(maps, p, stream);
+  return pack ? launch_instance<false, true>(maps, p, stream) : launch_instance<false, false>(maps, p, stream);
 }
 
 }  // namespace mla

@@ -64,6 +64,11 @@ class Workload:
         return self.q_nope.shape[0]
 
     @property
+    def mtp_q_len(self) -> int:
+        """Tokens per request of a packed multi-token decode workload."""
+        return self.rows // self.batch if self.batch else 0
+
+    @property
     def num_kv_indices(self) -> int:
         return self.kv_indices.numel()
 
@@ -194,6 +199,17 @@ def make_prefill(q_lens: Sequence[int], prefixes: Sequence[int], num_qo_heads: i
                     qo_indptr=torch.tensor(qo, dtype=torch.int32))
 
 
+def make_mtp(kv_lens: Optional[Sequence[int]], q_len: int, num_qo_heads: int, page_size: int, seed: int,
+             kv_lens_fn=None, name: str = "mtp") -> Workload:
+    """Packed multi-token decode: every request has q_len new tokens at the end of its
+    kv_len keys (a prefill with q_lens = q_len and prefixes = kv_len - q_len, kind "mtp")."""
+    if kv_lens is None:
+        kv_lens = kv_lens_fn(torch.Generator().manual_seed(seed))
+    w = make_prefill([q_len] * len(kv_lens), [k - q_len for k in kv_lens], num_qo_heads=num_qo_heads,
+                     page_size=page_size, seed=seed, name=name)
+    return dataclasses.replace(w, kind="mtp")
+
+
 def poison_unreferenced(w: Workload, value: float = float("nan")) -> Workload:
     """Return a copy whose cache slots not named in kv_indices hold ``value``."""
     ckv = w.ckv_cache.clone()
@@ -241,12 +257,22 @@ def prefill_causal_h128() -> Workload:
                         page_size=64, seed=1005, name="prefill_causal_h128")
 
 
+def mtp_b64_h16_q4_ps64() -> Workload:
+    """Packed multi-token decode: batch 64, 16 heads, 4 tokens per request (64 rows per
+    tile), page 64, kv lens uniform in [1024, 8192]."""
+    def lens(gen):
+        return torch.randint(1024, 8193, (64,), generator=gen).tolist()
+    return make_mtp(None, 4, num_qo_heads=16, page_size=64, seed=1006, kv_lens_fn=lens,
+                    name="mtp_b64_h16_q4_ps64")
+
+
 NAMED = {
     "decode_b4_h16_ps64": decode_b4_h16_ps64,
     "decode_b64_h128_ps64": decode_b64_h128_ps64,
     "decode_b128_h128_ps1": decode_b128_h128_ps1,
     "decode_b32_h128_skew": decode_b32_h128_skew,
     "prefill_causal_h128": prefill_causal_h128,
+    "mtp_b64_h16_q4_ps64": mtp_b64_h16_q4_ps64,
 }
 
 

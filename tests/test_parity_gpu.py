@@ -25,9 +25,7 @@ LSE_TOL = 1e-3
 def run_gpu(lib, w, **kw):
     require_gpu()
     wd = w.to("cuda")
-    dims = lib.make_dims(w.batch, w.num_qo_heads, w.num_pages, w.page_size, w.num_kv_indices,
-                         total_q=w.rows if w.kind == "prefill" else 0, num_workers=kw.get("num_workers", 0))
-    ws = torch.zeros(lib.workspace_bytes(dims, w.kind == "prefill"), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(lib.workload_workspace_bytes(w, kw.get("num_workers", 0)), dtype=torch.uint8, device="cuda")
     out, lse = lib.run_workload(wd, workspace=ws, **kw)
     assert lib.read_device_status(ws) == 0, "device status word reports an error (bounded wait gave up?)"
     return out.float().cpu().numpy(), lse.cpu().numpy()
@@ -84,6 +82,44 @@ def test_decode_small_pages_with_runs(lib, layout):
             idx[t0:t0 + 64] = idx[t0:t0 + 64].flip(0)
     w = dataclasses.replace(w, kv_indices=idx)
     check_full(lib, w)
+
+
+# ------------------------------------------------- packed multi-token decode
+
+@pytest.mark.parametrize("q_len,heads,ps,lens", [
+    (2, 16, 64, [2, 63, 64, 65, 700, 129]),   # 32 rows per tile
+    (4, 32, 64, [4, 5, 200, 1000, 64]),       # 128 rows per tile
+    (3, 16, 1, [3, 90, 300]),                 # small pages (copied tiles)
+    (1, 128, 64, [1, 100, 640]),              # one token: plain decode through the packed path
+])
+def test_mtp_small(lib, q_len, heads, ps, lens):
+    w = wl.make_mtp(lens, q_len, num_qo_heads=heads, page_size=ps, seed=2800 + q_len * heads + ps)
+    check_full(lib, w)
+
+
+@pytest.mark.parametrize("workers", [1, 3, 40])
+def test_mtp_split_rows(lib, workers):
+    """Requests split across workers so that some tokens see no key of a segment
+    (the first token's horizon ends one key before the last token's)."""
+    w = wl.make_mtp([4 * 64 + 1, 130, 2000, 67], 4, num_qo_heads=32, page_size=64, seed=2810)
+    check_full(lib, w, num_workers=workers)
+
+
+def test_mtp_rejects_too_many_rows(lib):
+    require_gpu()
+    w = wl.make_mtp([10, 20], 2, num_qo_heads=128, page_size=64, seed=2811).to("cuda")
+    with pytest.raises(lib.MlaError):
+        lib.run_workload(w)
+
+
+def test_full_size_mtp_sampled(lib):
+    """The packed multi-token benchmark workload at full size, checked on sampled requests."""
+    w = wl.by_name("mtp_b64_h16_q4_ps64")
+    out, lse = run_gpu(lib, w)
+    qo = w.qo_indptr.tolist()
+    rows = [r for b in (0, 17, 63) for r in range(qo[b], qo[b + 1])]
+    ref_out, ref_lse = oracle_run(w, rows=rows)
+    assert_close(out[rows], lse[rows], ref_out[rows], ref_lse[rows], "mtp_b64_h16_q4_ps64 sampled")
 
 
 def test_decode_empty_request(lib):
