@@ -91,3 +91,26 @@ def test_status_strings(lib):
     for code in range(0, -10, -1):
         s = lib.string_of(code)
         assert s.startswith("MLA_")
+
+
+def _mtp(lib, dims, q_len, ws_bytes=1 << 30):
+    v = ctypes.c_void_p
+    return lib.lib().mla_paged_decode_mtp(v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), v(FAKE), 0.1, v(FAKE),
+                                          v(FAKE), ctypes.byref(dims), q_len, v(FAKE), ws_bytes, 0, None)
+
+
+def test_mtp_host_argument_errors(lib):
+    assert _mtp(lib, _dims(lib, num_qo_heads=16), 0) == -2          # q_len < 1
+    assert _mtp(lib, _dims(lib, num_qo_heads=16), 9) == -2          # 9 x 16 rows > 128
+    assert _mtp(lib, _dims(lib, num_qo_heads=128), 2) == -2
+    assert _mtp(lib, _dims(lib, num_qo_heads=16), 8, ws_bytes=16) == -4
+    assert _mtp(lib, _dims(lib, num_qo_heads=16, batch=0, num_kv_indices=0), 4) == 0
+
+
+def test_mtp_workspace_is_decode_workspace_of_packed_rows(lib):
+    for h, q in ((16, 4), (32, 4), (8, 3), (128, 1)):
+        a = lib.workspace_bytes_mtp(_dims(lib, num_qo_heads=h), q)
+        b = lib.workspace_bytes(_dims(lib, num_qo_heads=h * q), False)
+        assert a == b > 0
+    assert lib.workspace_bytes_mtp(_dims(lib, num_qo_heads=16), 9) == 0
+    assert lib.workspace_bytes_mtp(_dims(lib, num_qo_heads=16), 0) == 0
