@@ -606,24 +606,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
     auto fetch = [&]() -> bool {
       if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout)) return false;
       tc_fence_after();
-      {
-        uint32_t sn[32];
-        tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
-        tmem_ld_wait();
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          uint32_t v[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) v[e] = round24(sn[4 * g + e]);
-          pack24(v, &nxt[3 * g]);
-        }
-      }
+      uint32_t sn[32];
+      tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
+      // The tile's descriptor: its KV_FULL phase has completed (QK read the tile); the
+      // barrier probe overlaps the TMEM load.
+      const bool kv_ok =
+          mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout);
+      tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(S_EMPTY));
-      // The tile's descriptor: its KV_FULL phase has completed (QK read the tile).
-      if (!mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout))
-        return false;
+      if (lane == 0) mbar_arrive(bar(S_EMPTY));  // the next QK may overwrite S now
+      if (!kv_ok) return false;
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        uint32_t v[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = round24(sn[4 * g + e]);
+        pack24(v, &nxt[3 * g]);
+      }
       q_pending = desc[jf % kDescRing].next_row;
       ++jf;
       return true;
@@ -667,52 +667,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       // can leave the moment tile j's has arrived.
       if (jf < ntiles && !fetch()) break;
       if (!mbar_wait<true>(bar(X_FULL0 + 8 * b + warp), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
-      float s[32];
-      {
-        uint32_t pw[24];
+      // The peer's piece of tile j is here: load it, then send tile j+1 at once (the send
+      // is what the peer waits for, so the unpacking below stays off that path).  The
+      // loads are issued before the stores; the buffer is rewritten only with the peer's
+      // tile j+2, which leaves the peer after tile j+1 has arrived there.
+      uint32_t pw[24];
 #pragma unroll
-        for (int c = 0; c < 6; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(smem + kOffX + b * kXBytes + piece + c * 512);
-          pw[4 * c] = v.x;
-          pw[4 * c + 1] = v.y;
-          pw[4 * c + 2] = v.z;
-          pw[4 * c + 3] = v.w;
-        }
-#pragma unroll
-        for (int g = 0; g < 8; ++g) {
-          float a[4], c4[4];
-          unpack24(&own[3 * g], a);
-          unpack24(&pw[3 * g], c4);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) s[4 * g + e] = a[e] + c4[e];
-        }
-      }
+      for (int c = 0; c < 6; ++c)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(pw[4 * c]), "=r"(pw[4 * c + 1]), "=r"(pw[4 * c + 2]), "=r"(pw[4 * c + 3])
+                     : "r"(x_local + b * kXBytes + piece + c * 512)
+                     : "memory");
+      if (jf > j + 1) send_piece(j + 1, nxt);
       __syncwarp();
       if (lane == 0) mbar_arrive_expect_tx(bar(X_FULL0 + 8 * b + warp), kXWarpBytes);  // arm its next use
-      __syncwarp();
-      if (jf > j + 1) {
-        send_piece(j + 1, nxt);  // then send tile j+1
-        if (q_pending >= 0) {
-          write_q(q_pending);
-          q_pending = -1;
-        }
+      float s[32];
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        float a[4], c4[4];
+        unpack24(&own[3 * g], a);
+        unpack24(&pw[3 * g], c4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[4 * g + e] = a[e] + c4[e];
+      }
+      if (q_pending >= 0) {
+        write_q(q_pending);
+        q_pending = -1;
       }
       const int nvalid = min(kTileKeys, (kPack ? cd.len - lag : cd.len) - cd.t * kTileKeys) - 32 * half;
       // All 32 keys valid and a non-negative scale (the usual case): the maximum of the
       // scaled scores is the scaled maximum, and the scale folds into the exponent below.
       const bool full = nvalid >= 32 && scale >= 0.f;
-      float mx = -INFINITY;
-      if (full) {
+      if (!full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) mx = fmaxf(mx, s[k]);
-        mx *= scale;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = k < nvalid ? s[k] * scale : -INFINITY;
-          mx = fmaxf(mx, s[k]);
-        }
+        for (int k = 0; k < 32; ++k) s[k] = k < nvalid ? s[k] * scale : -INFINITY;
       }
+      float mx;
+      {  // maximum as a tree (short dependency chains)
+        float m8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(fmaxf(s[k], s[k + 8]), fmaxf(s[k + 16], s[k + 24]));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m8[k] = fmaxf(m8[k], m8[k + 4]);
+        mx = fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3]));
+      }
+      if (full) mx *= scale;
       red[(b * 2 + half) * 128 + row] = mx;
       pair_sync(warp);
       mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
@@ -728,7 +727,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         rescale = true;
       }
       uint32_t pk[16];
-      float sum = 0.f;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
       // A packed token can see no key of a split segment (m_ref = -inf): its P is zero.
       const float mref = (kPack && m_ref == -INFINITY) ? 0.f : m_ref;
       if (full) {
@@ -736,7 +735,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         for (int k = 0; k < 16; ++k) {
           const float a = fast_exp2(fmaf(s[2 * k], scale, -mref));
           const float bb = fast_exp2(fmaf(s[2 * k + 1], scale, -mref));
-          sum += a + bb;
+          sum4[k & 3] += a + bb;
           __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
           pk[k] = *reinterpret_cast<uint32_t*>(&h);
         }
@@ -745,12 +744,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         for (int k = 0; k < 16; ++k) {
           const float a = fast_exp2(s[2 * k] - mref);
           const float bb = fast_exp2(s[2 * k + 1] - mref);
-          sum += a + bb;
+          sum4[k & 3] += a + bb;
           __nv_bfloat162 h = __floats2bfloat162_rn(a, bb);
           pk[k] = *reinterpret_cast<uint32_t*>(&h);
         }
       }
-      l += sum;
+      l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // P is single-buffered: the previous tile's P.V must be done (it also settles O).
       if (j >= 1 && !mbar_wait(bar(PV_DONE), (j - 1) & 1, abort, p.status, kStatusTimeout)) break;
       tc_fence_after();
