@@ -55,7 +55,8 @@ enum mla_status {
   MLA_ERR_BAD_INDEX = -6,  /* (device status) MLA_VALIDATE found bad indptr/indices        */
   MLA_ERR_TIMEOUT = -7,    /* (device status) a bounded wait inside a kernel gave up       */
   MLA_ERR_CUDA = -8,       /* a CUDA runtime/driver call failed (device query, TMA encode) */
-  MLA_ERR_UNSUPPORTED = -9 /* no sm_103a-class device is current                           */
+  MLA_ERR_UNSUPPORTED = -9, /* no sm_103a-class device is current                          */
+  MLA_ERR_INTERNAL = -10   /* (device status) a kernel found an internal invariant broken  */
 };
 
 /* Flags (bitwise OR). */
@@ -88,10 +89,11 @@ typedef struct mla_dims {
  *   out        [batch, H, 512] bf16 (written)   lse [batch, H] fp32, natural log (written)
  *   workspace  device scratch of at least mla_workspace_bytes(dims, 0) bytes, caller-owned;
  *              it holds split-KV partial results, merge counters and the device status
- *              word.  Zero-fill it before its first use; every call leaves the counters
- *              at zero again, but after a call that reported a device error (read with
- *              mla_read_device_status) zero-fill it once more.  Calls that share a
- *              workspace must not overlap on the GPU.
+ *              word.  Zero-fill it once before its first use (the status word, its first
+ *              4 bytes, only accumulates error bits until mla_read_device_status clears
+ *              it); everything else is rewritten by every call, so one workspace may serve
+ *              calls with different sizes, worker counts or head counts.  Calls that share
+ *              a workspace must not overlap on the GPU.
  *   flags      MLA_VALIDATE or 0;  stream: cudaStream_t
  * Returns MLA_OK or a negative mla_status; nothing is launched on an argument error.
  */
@@ -148,15 +150,23 @@ int mla_paged_decode_mtp(const void* q_nope, const void* q_pe, const void* ckv_c
  * dims->num_workers == 0 the call uses one worker per SM pair, or fewer if their
  * partial results would not fit in the 32 MiB; an explicit num_workers whose scratch
  * needs more returns MLA_ERR_WORKSPACE.  flags must be 0 (the device status word is not
- * readable through this entry point), else MLA_ERR_DIMS.  All calls share the array and
- * it keeps the last call's contents: calls that overlap on the GPU race.  The first
- * call on each device looks up the array's address (with that device current); make it
- * before any stream capture.  The call itself allocates nothing.
+ * read through the status call below instead), else MLA_ERR_DIMS.  All calls share the
+ * array and it keeps the last call's contents: calls that overlap on the GPU race.
+ * Nothing else carries over between calls (each call clears the status word and zeroes
+ * the merge counters it uses).  The first call on each device looks up the array's
+ * address (with that device current); make it before any stream capture.  The call
+ * itself allocates nothing.
  */
 int mla_paged_decode_noalloc(const void* q_nope, const void* q_pe, const void* ckv_cache,
                              const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
                              float sm_scale, void* out, float* lse, const mla_dims* dims, int flags,
                              void* stream);
+
+/* Device status of the most recent mla_paged_decode_noalloc call on the current device:
+ * synchronises `stream`, reads and clears the status word in the library's static
+ * scratch and returns MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_INTERNAL (as
+ * mla_read_device_status does for a caller's workspace).  No counterpart on the pages. */
+int mla_noalloc_read_status(void* stream);
 
 /* Workspace bytes a call with these dims needs (0 on invalid dims).  With
  * dims->num_workers == 0 it queries the current device's SM count. */
@@ -174,8 +184,8 @@ int mla_default_num_workers(void);
 const char* mla_status_string(int status);
 
 /* Synchronises `stream`, reads the device status word kept in `workspace` (MLA_OK,
- * MLA_ERR_BAD_INDEX or MLA_ERR_TIMEOUT), clears it, and returns it.  Returns
- * MLA_ERR_CUDA if the synchronisation itself reports an error. */
+ * MLA_ERR_BAD_INDEX, MLA_ERR_TIMEOUT or MLA_ERR_INTERNAL), clears it, and returns it.
+ * Returns MLA_ERR_CUDA if the synchronisation itself reports an error. */
 int mla_read_device_status(void* workspace, void* stream);
 
 /* Kernel timing for benchmarks.  When enabled, every call records CUDA events on its

@@ -21,7 +21,7 @@ MLA_VALIDATE = 1
 
 _STATUS = {0: "MLA_OK", -1: "MLA_ERR_NULL", -2: "MLA_ERR_DIMS", -3: "MLA_ERR_ALIGN",
            -4: "MLA_ERR_WORKSPACE", -5: "MLA_ERR_LAUNCH", -6: "MLA_ERR_BAD_INDEX",
-           -7: "MLA_ERR_TIMEOUT", -8: "MLA_ERR_CUDA", -9: "MLA_ERR_UNSUPPORTED"}
+           -7: "MLA_ERR_TIMEOUT", -8: "MLA_ERR_CUDA", -9: "MLA_ERR_UNSUPPORTED", -10: "MLA_ERR_INTERNAL"}
 
 
 class MlaError(RuntimeError):
@@ -59,6 +59,7 @@ _SIGNATURES = [
     ("mla_default_num_workers", ctypes.c_int, []),
     ("mla_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("mla_read_device_status", ctypes.c_int, [_P, _P]),
+    ("mla_noalloc_read_status", ctypes.c_int, [_P]),
     ("mla_profile_enable", ctypes.c_int, [ctypes.c_int]),
     ("mla_profile_read", ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int)]),
@@ -287,6 +288,16 @@ def mla_paged_decode_noalloc(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_i
     if st != 0:
         raise MlaError(st, "mla_paged_decode_noalloc")
     return out, lse
+
+
+def noalloc_read_status(device=None, stream=None) -> int:
+    """Synchronise, read and clear the status word of the most recent
+    ``mla_paged_decode_noalloc`` call on ``device``."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        return int(lib().mla_noalloc_read_status(ctypes.c_void_p(stream.cuda_stream)))
 
 
 def read_device_status(workspace: torch.Tensor, stream=None) -> int:

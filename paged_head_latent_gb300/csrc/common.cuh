@@ -16,6 +16,7 @@ constexpr int kMaxHeads = 128;
 // Bits of the device status word (workspace offset 0).
 constexpr uint32_t kStatusBadIndex = 1u;
 constexpr uint32_t kStatusTimeout = 2u;
+constexpr uint32_t kStatusInternal = 4u;  // an internal invariant failed (misaligned shared memory)
 
 struct MlaParams {
   const __nv_bfloat16* q_nope;  // [rows, H, 512]
@@ -37,7 +38,7 @@ struct MlaParams {
   // workspace
   uint32_t* status;         // device status word
   CombineRecord* records;   // [G]
-  int* merge_count;         // [G][ceil(H/8)] chunk-merge arrivals (zero between calls)
+  int* merge_count;         // [G][ceil(H/8)] chunk-merge arrivals (zeroed by the attention kernel)
   float* part_lse;          // [G][2][H]  base-2 lse of partial fragments
   float* part_o;            // [G][2][H][512] normalised partial outputs
   // Packed multi-token decode (0 otherwise): each request has mtp_q query tokens of
@@ -49,7 +50,7 @@ struct MlaParams {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace layout: [status (256 B)] [records: G x 20 B] [merge counters] [part_lse] [part_o].
+// Workspace layout: [status (256 B)] [records: G x 24 B] [merge counters] [part_lse] [part_o].
 struct WorkspaceLayout {
   size_t records, merge_count, part_lse, part_o, total;
   __host__ __device__ WorkspaceLayout(int G, int H) {

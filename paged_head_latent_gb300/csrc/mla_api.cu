@@ -165,7 +165,9 @@ struct ProfileState {
   size_t used = 0;              // triples in use
 };
 ProfileState g_prof;
+std::mutex g_prof_mu;
 
+// Called with g_prof_mu held.
 cudaEvent_t* profile_slot() {
   if (!g_prof.on) return nullptr;
   size_t need = (g_prof.used + 1) * 3;
@@ -245,7 +247,11 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   if (flags & MLA_VALIDATE) {
     if (mla::launch_validate(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
   }
+  // Benchmark timing (off unless mla_profile_enable): the lock keeps the event list
+  // consistent when calls come from several host threads.
+  std::unique_lock<std::mutex> prof_lk(g_prof_mu);
   cudaEvent_t* ev = profile_slot();
+  if (!ev) prof_lk.unlock();
   if (ev) cudaEventRecord(ev[0], stream);
   {
     mla::TmaMaps maps;
@@ -322,6 +328,7 @@ const char* mla_status_string(int status) {
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded wait in a kernel gave up";
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA: a CUDA runtime call failed";
     case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: current device is not sm_103";
+    case MLA_ERR_INTERNAL: return "MLA_ERR_INTERNAL: a kernel found an internal invariant broken (shared memory misaligned)";
     default: return "unknown mla_status";
   }
 }
@@ -340,18 +347,21 @@ int mla_read_device_status(void* workspace, void* stream_ptr) {
         cudaStreamSynchronize(stream) != cudaSuccess)
       return MLA_ERR_CUDA;
   }
+  if (word & mla::kStatusInternal) return MLA_ERR_INTERNAL;
   if (word & mla::kStatusTimeout) return MLA_ERR_TIMEOUT;
   if (word & mla::kStatusBadIndex) return MLA_ERR_BAD_INDEX;
   return MLA_OK;
 }
 
 int mla_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
   g_prof.on = on != 0;
   g_prof.used = 0;
   return MLA_OK;
 }
 
 int mla_profile_read(double* main_ms, double* combine_ms, int* calls) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
   double a = 0, b = 0;
   for (size_t i = 0; i < g_prof.used; ++i) {
     cudaEvent_t* e = &g_prof.ev[i * 3];

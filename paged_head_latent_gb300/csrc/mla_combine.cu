@@ -12,8 +12,8 @@
 // a fragment) is merged in two levels so that many CTAs share it: the CTA of
 // the last worker of each chunk of kChunk consecutive fragments merges that chunk into
 // the chunk's first fragment slot, then counts itself in; the CTA that arrives last
-// merges the chunk results, in chunk order, and resets the counter to zero for the next
-// call (the workspace starts zero-filled).
+// merges the chunk results, in chunk order.  The attention kernel zeroes the counters at
+// the start of every call.
 #include "common.cuh"
 #include "launch.h"
 
@@ -204,7 +204,6 @@ __global__ void __launch_bounds__(kCombineThreads) mla_combine_kernel(MlaParams 
   }
   __syncthreads();
   if (!last) return;
-  if (threadIdx.x == 0) p.merge_count[rec.w_last * ((p.heads + 7) / 8) + blockIdx.y] = 0;
   if (h >= p.heads) return;
   __threadfence();
   // Level 2: chunk k's result sits in its first existing fragment's slot.

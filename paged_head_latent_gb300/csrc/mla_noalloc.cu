@@ -12,7 +12,10 @@
 //    until the process exits;
 //  - all calls share the one array, and it keeps the previous call's contents, so
 //    calls that overlap on the GPU (different streams, or several host threads
-//    without ordering) race and corrupt each other's partial results;
+//    without ordering) race and corrupt each other's partial results.  Nothing a call
+//    relies on carries over from the call before: the status word is cleared here and
+//    the attention kernel zeroes the merge counters, whatever sizes the previous call
+//    had;
 //  - the array's address is looked up once per device (cudaGetSymbolAddress) by the
 //    first call made on that device, with that device current; make that first call
 //    before any stream capture.
@@ -77,11 +80,21 @@ extern "C" int mla_paged_decode_noalloc(const void* q_nope, const void* q_pe, co
   void* scratch = nullptr;
   const int st = scratch_for_current_device(&scratch);
   if (st != MLA_OK) return st;
-  // The status word must start at zero (kernels only set bits in it).
+  // The status word starts every call at zero (kernels only set bits in it), so after a
+  // call mla_noalloc_read_status reports that call's device errors.
   if (cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();
     return MLA_ERR_LAUNCH;
   }
   return mla_paged_decode(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale, out, lse, &d,
                           scratch, kNoAllocScratchBytes, 0, stream);
+}
+
+// The device status word of the most recent call on the current device (MLA_OK,
+// MLA_ERR_TIMEOUT, MLA_ERR_INTERNAL), read and cleared after synchronising `stream`.
+extern "C" int mla_noalloc_read_status(void* stream) {
+  void* scratch = nullptr;
+  const int st = scratch_for_current_device(&scratch);
+  if (st != MLA_OK) return st;
+  return mla_read_device_status(scratch, stream);
 }

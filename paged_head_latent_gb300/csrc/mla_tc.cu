@@ -53,6 +53,8 @@
 //   warp 9     issues S = Q.K^T (one thread) and owns TMEM
 //   warp 10    issues O += P.V (one thread); tcgen05.mma issue blocks while the tensor
 //              pipe is busy, so the two products get separate issuing threads.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -214,7 +216,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
 
   if (threadIdx.x == 0) {
     misc.abort = (sbase & 1023u) ? 1 : 0;  // swizzled tiles need 1 KB alignment
-    if (misc.abort) atomicOr(p.status, kStatusTimeout);
+    if (misc.abort) atomicOr(p.status, kStatusInternal);
     mbar_init(bar(Q_FULL), kSoftmaxWarps);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(KV_FULL0 + s), kGather ? 2 : 1);  // one arrival per copy warp
@@ -256,6 +258,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
     }
     if (w == 0 && rank == 0) warp_write_empty_rows(p);
+    // This worker's row of merge counters starts every call at zero: the merge kernel
+    // counts on it only after this grid has completed, so no state is carried from call
+    // to call (nor from a call with another worker count or head count).
+    if (rank == 0)
+      for (int g = lane; g < (p.heads + 7) / 8; g += 32) p.merge_count[(size_t)w * ((p.heads + 7) / 8) + g] = 0;
   }
   tc_fence_before();
   __syncthreads();
@@ -853,14 +860,21 @@ uint32_t tc_smem_bytes() { return kSmemBytes; }
 namespace {
 template <bool kGather, bool kPack>
 cudaError_t launch_instance(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream) {
+  // The shared-memory attribute is set once per device and instance; calls may come from
+  // any host thread.
+  static std::mutex mu;
   static bool configured[64] = {};
   int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !configured[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<kGather, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
-    configured[dev] = true;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (!configured[dev]) {
+      cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<kGather, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)kSmemBytes);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
   }
   mla_tc_kernel<kGather, kPack><<<2 * p.workers, kGather ? kThreadsGather : kThreads, kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
