@@ -1,13 +1,17 @@
-"""Benchmark of the paged-MLA decode hot path on GB300 (one JSON line on stdout).
+"""Benchmark of the paged-MLA hot path on GB300 (one JSON line on stdout).
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-A step is one call of the whole path (split-KV attention kernel + combine kernel)
-over one batch of the named synthetic workload, inputs resident in HBM.  Between
-timed steps L2 is flushed by writing a 256 MiB buffer; each step is timed with
-CUDA events on the launching stream.  ``value`` is microseconds per call.
-``e2e`` times the same call from pinned host buffers: host->device copies of every
-input, the call, and the device->host copy of out and lse.
+A step is one call of the whole path (split-KV attention kernel + merge kernel) over one
+batch of a named synthetic workload, inputs resident in HBM.  Before every timed step
+L2 is flushed by writing a 256 MiB buffer; each step is timed with CUDA events on the
+launching stream.  ``value`` is the median microseconds per call of the headline
+workload (decode, batch 128, 128 heads, page size 1, 4096 keys each: the largest
+single-GPU decode configuration); p10/p90 and the mean are reported beside it.
+``configs`` holds the same measurements for the other named workloads (the small
+decode, the page-64 decode, the skewed decode, the causal prefill).  ``e2e`` times the
+headline call from pinned host buffers: host->device copies of every input, the call,
+and the device->host copy of out and lse.
 
 --impl reference times the float64 CPU oracle on the host cores instead (bounded
 samples of the same workload, scaled to a whole call).
@@ -22,13 +26,15 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA paged decode µs/call, KV TB/s & TFLOP/s as % of GB300 roofline"
-DEFAULT_WORKLOAD = "decode_b64_h128_ps64"
+HEADLINE = "decode_b128_h128_ps1"
+SUB_WORKLOADS = ("decode_b4_h16_ps64", "decode_b64_h128_ps64", "decode_b32_h128_skew", "prefill_causal_h128")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -53,6 +59,12 @@ def algorithmic_work(w):
     nbytes = sum(w.kv_lens()) * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
     flops = keys * w.num_qo_heads * 2 * (576 + 512)
     return nbytes, flops, keys
+
+
+def config_of(w):
+    """The workload description both arms print (identical keys and values)."""
+    return {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads, "page_size": w.page_size,
+            "visible_keys": w.visible_keys()}
 
 
 # The sources that define the attention kernel; the recorded DRAM traffic is valid only
@@ -83,6 +95,12 @@ def recorded_traffic(workload):
     return e.get("dram_bytes_per_launch")
 
 
+def percentiles(vals):
+    v = sorted(vals)
+    q = lambda f: v[min(len(v) - 1, max(0, int(round(f * (len(v) - 1)))))]
+    return {"median": statistics.median(v), "p10": q(0.10), "p90": q(0.90), "mean": sum(v) / len(v)}
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
 
@@ -93,7 +111,7 @@ class ClockSampler:
     def __init__(self, uuid=None):
         self.uuid = uuid
         self.proc = None
-        self.path = os.path.join("/tmp", f"mla_clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"mla_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
@@ -138,7 +156,7 @@ class ClockSampler:
                 if any(r[4].replace(".", "").isdigit() for r in rows) else None}
 
 
-# ------------------------------------------------------------------ reference arm
+# ------------------------------------------------------------------ CPU oracle legs
 
 def time_oracle(w, budget_s, max_rows=None):
     """Run the oracle on whole query rows of ``w`` (all heads) until ``budget_s`` of CPU
@@ -177,6 +195,49 @@ def cores_used():
         return os.cpu_count()
 
 
+def cpu_baseline(w, budget_s):
+    keys = w.visible_keys()
+    secs, ck, cr = time_oracle(w, budget_s)
+    return {"value": secs / max(ck, 1) * keys * 1e6, "unit": "us/call", "cores": cores_used(), "kind": "oracle",
+            "sample": f"{cr} of {w.rows} query rows (all heads) of {w.name}, {ck} of {keys} visible keys, "
+                      f"{secs:.1f} s, scaled to the whole call"}
+
+
+_SINGLE_THREAD = r"""
+import json, sys, time
+import numpy as np
+sys.path.insert(0, sys.argv[2])
+import oracle
+d = np.load(sys.argv[1])
+best = None
+for _ in range(3):
+    t0 = time.perf_counter()
+    oracle.mla_decode(d["q_nope"], d["q_pe"], d["ckv"], d["kpe"], d["indptr"], d["indices"], float(d["scale"]))
+    t = time.perf_counter() - t0
+    best = t if best is None or t < best else best
+print(json.dumps({"us": best * 1e6}))
+"""
+
+
+def single_thread_oracle_us(w):
+    """The whole call of a (small) decode workload on one host thread: the oracle runs in
+    a child process whose BLAS is limited to one thread; min of three runs."""
+    import numpy as np
+    with tempfile.TemporaryDirectory() as d:
+        path = os.path.join(d, "inputs.npz")
+        np.savez(path, q_nope=w.q_nope.float().numpy(), q_pe=w.q_pe.float().numpy(),
+                 ckv=w.ckv_cache.float().numpy(), kpe=w.kpe_cache.float().numpy(),
+                 indptr=w.kv_indptr.numpy(), indices=w.kv_indices.numpy(), scale=w.sm_scale)
+        env = dict(os.environ)
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[k] = "1"
+        r = subprocess.run([sys.executable, "-c", _SINGLE_THREAD, path, ROOT], capture_output=True, text=True,
+                           env=env, timeout=300)
+        if r.returncode != 0:
+            return None
+        return json.loads(r.stdout.strip().splitlines()[-1])["us"]
+
+
 def max_over_ranks(value, world, device=None):
     """The largest value over all ranks (every rank gets it); the value itself at N = 1."""
     if world <= 1:
@@ -209,8 +270,7 @@ def reference_arm(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": us_per_call, "unit": "us/call",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": us_per_call / 1e3,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads,
-                                        "page_size": w.page_size, "visible_keys": total_keys},
+        "data": "synthetic", "config": config_of(w),
         "kv_tbs": nbytes / (us_per_call * 1e-6) / 1e12, "tflops": flops / (us_per_call * 1e-6) / 1e12,
         "cpu_baseline": {"value": us_per_call, "unit": "us/call", "cores": cores_used(), "kind": "oracle",
                          "sample": sample},
@@ -221,45 +281,58 @@ def reference_arm(args, rank, world):
 
 # ------------------------------------------------------------------------ our arm
 
-def our_arm(args, rank, world, local_rank):
-    import torch
-    import paged_head_latent_gb300 as mla
-    from paged_head_latent_gb300 import workloads as wl
+def roofline_of(w_cpu, kernel_ms, peaks, peak_kind):
+    """Roofline of the dominant (attention) kernel: algorithmic bytes or flops per launch
+    over its CUDA-event duration, against the measured HBM copy bandwidth or bf16 GEMM
+    rate, whichever bound the operator's work has (a kernel that runs for milliseconds
+    is compared with the sustained bf16 figure, a short one with the burst figure)."""
+    nbytes, flops, _ = algorithmic_work(w_cpu)
+    hbm = float(peaks["hbm_gbs"])
+    tc = float(peaks["bf16_tflops"])
+    ach_gbs = nbytes / (kernel_ms * 1e-3) / 1e9
+    ach_tflops = flops / (kernel_ms * 1e-3) / 1e12
+    tensor_bound = flops / (tc * 1e12) > nbytes / (hbm * 1e9)
+    common = {"peak_kind": peak_kind, "kernel": "attention kernel (mla_tc_kernel)", "kernel_us": kernel_ms * 1e3,
+              "hbm_gbs": ach_gbs, "hbm_frac": ach_gbs / hbm, "tensor_tflops": ach_tflops, "tensor_frac": ach_tflops / tc,
+              "algorithmic_bytes": nbytes, "algorithmic_flops": flops}
+    if tensor_bound:
+        tc_peak = float(peaks.get("bf16_tflops_sustained", tc)) if kernel_ms > 1.0 else tc
+        return {"bound": "tensor", "achieved": ach_tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                "frac": ach_tflops / tc_peak, "traffic": recorded_traffic(w_cpu.name),
+                "peak_figure": "sustained" if kernel_ms > 1.0 else "burst", **common}
+    return {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s", "frac": ach_gbs / hbm,
+            "traffic": recorded_traffic(w_cpu.name), **common}
 
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    w_cpu = wl.by_name(args.workload)
+
+def measure(mla, w_cpu, dev, stream, flush, steps, warmup, world, clocks_uuid=None, e2e=False, quick=False):
+    """Time `steps` calls of the path on `w_cpu` (inputs resident on `dev`, L2 flushed
+    before every call); returns per-call statistics, per-kernel times and, with e2e,
+    the end-to-end time from pinned host buffers."""
+    import torch
     w = w_cpu.to(dev)
-    nbytes, flops, keys = algorithmic_work(w_cpu)
-    stream = torch.cuda.Stream(dev)
     out = torch.empty(w.rows, w.num_qo_heads, 512, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(w.rows, w.num_qo_heads, dtype=torch.float32, device=dev)
-    ws = None
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-
     with torch.cuda.stream(stream):
         ws = torch.zeros(mla.workload_workspace_bytes(w), dtype=torch.uint8, device=dev)
-        # The C-ABI call with its arguments checked and marshalled once.
-        call = mla.bind_workload(w, out, lse, ws, stream)
-        for _ in range(max(args.warmup, 3)):
+        call = mla.bind_workload(w, out, lse, ws, stream)  # arguments checked and marshalled once
+        for _ in range(max(warmup, 3)):
             flush.fill_(1)
             call()
     stream.synchronize()
-
-    uuid = None
-    try:
-        uuid = str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        pass
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    res = {}
+    clocks = ClockSampler(clocks_uuid) if clocks_uuid is not False else None
     wall0 = time.perf_counter()
-    with ClockSampler(uuid) as clocks:
+    torch.cuda.nvtx.range_push(f"timed {w.name}")
+    if clocks:
+        clocks.__enter__()
+    try:
         with torch.cuda.stream(stream):
-            for i in range(args.steps):
+            for i in range(steps):
                 flush.fill_(i & 0xFF)
                 starts[i].record(stream)
                 call()
@@ -267,105 +340,138 @@ def our_arm(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
-        # keep sampling long enough for a few readings when the timed loop was short
-        while not args.quick and time.perf_counter() - wall0 < 1.0:
+        # keep sampling clocks long enough for a few readings when the timed loop was short
+        while clocks and not quick and time.perf_counter() - wall0 < 1.0:
             with torch.cuda.stream(stream):
                 for _ in range(20):
                     call()
             stream.synchronize()
-    wall_timed = time.perf_counter() - wall0
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
-    # Per-kernel durations: the same K steps again with the library's CUDA events around
-    # each kernel on the launching stream (kept out of the first pass, whose step time
+    finally:
+        if clocks:
+            clocks.__exit__()
+        torch.cuda.nvtx.range_pop()
+    res["wall_s_timed_loop"] = time.perf_counter() - wall0
+    step_us = [s.elapsed_time(e) * 1e3 for s, e in zip(starts, ends)]
+    res["us"] = percentiles(step_us)
+    res["us"]["median"] = max_over_ranks(res["us"]["median"], world, dev)
+    if clocks:
+        res["clocks"] = clocks.summary()
+    # Per-kernel durations: the same steps again with the library's CUDA events around
+    # each kernel on the launching stream (kept out of the first pass, whose call time
     # they would lengthen by separating the two kernels).
     torch.cuda.synchronize(dev)
     mla.profile_enable(True)
     with torch.cuda.stream(stream):
-        for i in range(args.steps):
+        for i in range(steps):
             flush.fill_(i & 0xFF)
             call()
     torch.cuda.synchronize(dev)
     main_ms, comb_ms, ncalls = mla.profile_read()
     mla.profile_enable(False)
-    main_avg_ms = main_ms / max(ncalls, 1)
-    comb_avg_ms = comb_ms / max(ncalls, 1)
+    res["kernel_ms"] = main_ms / max(ncalls, 1)
+    res["combine_ms"] = comb_ms / max(ncalls, 1)
+    if e2e:
+        host = {k: v.pin_memory() for k, v in w_cpu.tensors().items()}
+        dev_in = w.tensors()
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        res["h2d"] = sum(t.numel() * t.element_size() for t in host.values())
+        res["d2h"] = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        e2e_steps = 0 if quick else max(3, min(steps, 30))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        torch.cuda.nvtx.range_push(f"e2e {w.name}")
+        with torch.cuda.stream(stream):
+            for it in range(e2e_steps + 2 if e2e_steps else 0):
+                if it == 2:
+                    e0.record(stream)
+                for k, t in host.items():
+                    dev_in[k].copy_(t, non_blocking=True)
+                call()
+                out_h.copy_(out, non_blocking=True)
+                lse_h.copy_(lse, non_blocking=True)
+            if e2e_steps:
+                e1.record(stream)
+        stream.synchronize()
+        torch.cuda.nvtx.range_pop()
+        res["e2e_us"] = max_over_ranks(e0.elapsed_time(e1) / e2e_steps * 1e3 if e2e_steps else float("nan"),
+                                       world, dev)
+    del ws, out, lse, w
+    return res
 
-    # ---- end to end through the C ABI from pinned host buffers
-    host = {k: v.pin_memory() for k, v in w_cpu.tensors().items()}
-    dev_in = w.tensors()
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
-    e2e_steps = 0 if args.quick else max(3, min(args.steps, 30))
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for it in range(e2e_steps + 2 if e2e_steps else 0):
-            if it == 2:
-                e0.record(stream)
-            for k, t in host.items():
-                dev_in[k].copy_(t, non_blocking=True)
-            call()
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(lse, non_blocking=True)
-        if e2e_steps:
-            e1.record(stream)
-    stream.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps if e2e_steps else float("nan"), world, dev)
 
+def our_arm(args, rank, world, local_rank):
+    import torch
+    import paged_head_latent_gb300 as mla
+    from paged_head_latent_gb300 import workloads as wl
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    peaks, peak_kind = load_peaks()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+
+    w_cpu = wl.by_name(args.workload)
+    m = measure(mla, w_cpu, dev, stream, flush, args.steps, args.warmup, world, clocks_uuid=uuid,
+                e2e=True, quick=args.quick)
+    subs = []
+    if world == 1 and not args.no_sub:
+        for name in SUB_WORKLOADS:
+            if name == args.workload:
+                continue
+            ws_cpu = wl.by_name(name)
+            steps = min(args.steps, 20 if ws_cpu.kind == "prefill" else 100)
+            sm = measure(mla, ws_cpu, dev, stream, flush, steps, args.warmup, 1, clocks_uuid=False, quick=True)
+            nb, fl, _ = algorithmic_work(ws_cpu)
+            hbm, tc = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"])
+            roof_us = max(nb / (hbm * 1e9), fl / (tc * 1e12)) * 1e6
+            sub = {"workload": name, "config": config_of(ws_cpu), "steps": steps,
+                   "us_median": sm["us"]["median"], "us_p10": sm["us"]["p10"], "us_p90": sm["us"]["p90"],
+                   "us_mean": sm["us"]["mean"], "kernel_us": sm["kernel_ms"] * 1e3,
+                   "combine_us": sm["combine_ms"] * 1e3, "roofline_time_us": roof_us,
+                   "roofline_frac_call": roof_us / sm["us"]["median"],
+                   "roofline": roofline_of(ws_cpu, sm["kernel_ms"], peaks, peak_kind)}
+            if not args.no_cpu_baseline and not args.quick:
+                sub["cpu_baseline"] = cpu_baseline(ws_cpu, 3.0 if ws_cpu.kind == "prefill" else 2.0)
+                if name == "decode_b4_h16_ps64":
+                    st = single_thread_oracle_us(ws_cpu)
+                    sub["cpu_baseline_single_thread_us"] = st
+            subs.append(sub)
     if rank != 0:
         return
-    peaks, peak_kind = load_peaks()
-    hbm = float(peaks["hbm_gbs"])
-    tc = float(peaks["bf16_tflops"])
-    us = ms_per_step * 1e3
-    # Dominant kernel: the attention kernel.  Its algorithmic bytes per launch are the
-    # whole call's (the combine only re-reads split-KV partials, which are not algorithmic).
-    ach_gbs = nbytes / (main_avg_ms * 1e-3) / 1e9
-    ach_tflops = flops / (main_avg_ms * 1e-3) / 1e12
+    nbytes, flops, keys = algorithmic_work(w_cpu)
+    hbm, tc = float(peaks["hbm_gbs"]), float(peaks["bf16_tflops"])
+    us = m["us"]["median"]
     roof_time_us = max(nbytes / (hbm * 1e9), flops / (tc * 1e12)) * 1e6
-    # The bound of the dominant kernel: HBM for decode at these head counts, the tensor
-    # pipe for long causal prefill.  A kernel that runs for milliseconds is compared with
-    # the sustained bf16 figure, a short one with the burst figure.
-    tensor_bound = flops / (tc * 1e12) > nbytes / (hbm * 1e9)
-    common = {"peak_kind": peak_kind, "kernel": "attention (main) kernel", "kernel_us": main_avg_ms * 1e3,
-              "combine_us": comb_avg_ms * 1e3, "hbm_gbs": ach_gbs, "hbm_frac": ach_gbs / hbm,
-              "tensor_tflops": ach_tflops, "tensor_frac": ach_tflops / tc}
-    if tensor_bound:
-        tc_peak = float(peaks.get("bf16_tflops_sustained", tc)) if main_avg_ms > 1.0 else tc
-        roofline = {"bound": "tensor", "achieved": ach_tflops, "peak": tc_peak, "unit": "TFLOP/s",
-                    "frac": ach_tflops / tc_peak, "traffic": recorded_traffic(w_cpu.name),
-                    "peak_figure": "sustained" if main_avg_ms > 1.0 else "burst", **common}
-    else:
-        roofline = {"bound": "hbm", "achieved": ach_gbs, "peak": hbm, "unit": "GB/s", "frac": ach_gbs / hbm,
-                    "traffic": recorded_traffic(w_cpu.name), **common}
     cpu = None
     if world == 1 and not args.no_cpu_baseline and not args.quick:
-        secs, ck, cr = time_oracle(w_cpu, args.cpu_seconds)
-        cpu_us = secs / max(ck, 1) * keys * 1e6
-        cpu = {"value": cpu_us, "unit": "us/call", "cores": cores_used(), "kind": "oracle",
-               "sample": f"{cr} of {w_cpu.rows} query rows (all heads), {ck} of {keys} visible keys, "
-                         f"{secs:.1f} s, scaled to the whole call"}
+        cpu = cpu_baseline(w_cpu, args.cpu_seconds)
     line = {
         "metric": METRIC, "value": us, "unit": "us/call", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": False, "scaling": "weak",
+        "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": w_cpu.name, "batch": w_cpu.batch, "num_qo_heads": w_cpu.num_qo_heads,
-                   "page_size": w_cpu.page_size, "visible_keys": keys, "replicas": world,
-                   "l2": "flushed between steps (256 MiB write)", "accumulate": "fp32"},
+        "config": config_of(w_cpu),
+        "timing": {"us_median": us, "us_p10": m["us"]["p10"], "us_p90": m["us"]["p90"], "us_mean": m["us"]["mean"],
+                   "statistic": "value is the median of the per-step CUDA-event times",
+                   "l2": "flushed before every step (256 MiB write)", "accumulate": "fp32", "replicas": world,
+                   "kernel_timing": "attention and merge kernels timed with CUDA events in a second pass"},
         "kv_tbs": nbytes / (us * 1e-6) / 1e12,
         "tflops": flops / (us * 1e-6) / 1e12,
         "roofline_time_us": roof_time_us,
         "roofline_frac_call": roof_time_us / us,
-        "roofline": roofline,
+        "roofline": dict(roofline_of(w_cpu, m["kernel_ms"], peaks, peak_kind), combine_us=m["combine_ms"] * 1e3),
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_ms * 1e3, "unit": "us/call", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": m.get("e2e_us"), "unit": "us/call", "h2d_bytes_per_step": m.get("h2d"),
+                "d2h_bytes_per_step": m.get("d2h")},
         "gpu_launches": 2 * args.steps,
-        "clocks": clocks.summary(),
-        "wall_s_timed_loop": wall_timed,
-        "kernel_timing": "attention and merge kernels timed with CUDA events in a second pass of the same steps",
+        "clocks": m.get("clocks"),
+        "wall_s_timed_loop": m["wall_s_timed_loop"],
+        "configs": subs,
     }
     print(json.dumps(line), flush=True)
 
@@ -375,10 +481,11 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub", action="store_true", help="measure only the named workload")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no clock soak, no end-to-end leg, no CPU baseline")
     args = ap.parse_args()

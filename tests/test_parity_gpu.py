@@ -1,9 +1,8 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
 
 Tolerances (max-abs): 2e-2 on the bf16 output, 1e-3 on the fp32 natural-log lse.
-Small cases compare every element; the full-size named workloads run in the
-launch configuration the benchmark times and compare sampled rows, each
-computed by the oracle one at a time.
+Small cases and the full-size decode workloads compare every element; the full-size
+causal prefill compares a dense set of query rows (see below).
 """
 
 import dataclasses
@@ -14,7 +13,7 @@ import torch
 
 from paged_head_latent_gb300 import workloads as wl
 from tests.conftest import require_gpu
-from tests.oracle_io import oracle_rows_decode, oracle_rows_prefill, oracle_run
+from tests.oracle_io import oracle_run
 
 pytestmark = pytest.mark.gpu
 
@@ -110,16 +109,6 @@ def test_mtp_rejects_too_many_rows(lib):
     w = wl.make_mtp([10, 20], 2, num_qo_heads=128, page_size=64, seed=2811).to("cuda")
     with pytest.raises(lib.MlaError):
         lib.run_workload(w)
-
-
-def test_full_size_mtp_sampled(lib):
-    """The packed multi-token benchmark workload at full size, checked on sampled requests."""
-    w = wl.by_name("mtp_b64_h16_q4_ps64")
-    out, lse = run_gpu(lib, w)
-    qo = w.qo_indptr.tolist()
-    rows = [r for b in (0, 17, 63) for r in range(qo[b], qo[b + 1])]
-    ref_out, ref_lse = oracle_run(w, rows=rows)
-    assert_close(out[rows], lse[rows], ref_out[rows], ref_lse[rows], "mtp_b64_h16_q4_ps64 sampled")
 
 
 def test_decode_empty_request(lib):
@@ -263,34 +252,75 @@ def test_cuda_graph_capture(lib):
 
 
 # ------------------------------------------------------- full-size workloads
+#
+# The named full-size workloads run in the launch configuration the benchmark times
+# (default worker count, one call) and are compared with the oracle element by element:
+# every output and lse value of the three decode workloads and of the packed
+# multi-token workload; for the causal prefill (about 11 TFLOP in float64) every eighth
+# query row plus every row whose visible length sits at a 64-key tile boundary, the first
+# and last row of every request, and every row where a split-KV worker's range starts or
+# ends.
 
-def _sample_rows(n, extra=()):
-    rng = np.random.default_rng(7)
-    picks = set(int(x) for x in rng.choice(n, size=min(n, 6), replace=False))
-    picks.update(int(x) % n for x in extra)
-    return sorted(picks)
+FULL_DECODE = ["decode_b64_h128_ps64", "decode_b128_h128_ps1", "decode_b32_h128_skew"]
 
 
-@pytest.mark.parametrize("name", ["decode_b64_h128_ps64", "decode_b128_h128_ps1", "decode_b32_h128_skew"])
-def test_full_size_decode_sampled(lib, name):
+@pytest.mark.parametrize("name", FULL_DECODE)
+def test_full_size_decode_every_element(lib, name):
     w = wl.by_name(name)
     out, lse = run_gpu(lib, w)
-    lens = w.kv_lens()
-    rows = _sample_rows(w.batch, extra=(0, w.batch - 1, int(np.argmax(lens)), int(np.argmin(lens))))
-    ref = oracle_rows_decode(w, rows)
-    for r in rows:
-        assert_close(out[r], lse[r], ref[r][0], ref[r][1], f"{name} row {r}")
+    ref_out, ref_lse = oracle_run(w)
+    assert_close(out, lse, ref_out, ref_lse, name)
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
 
 
-def test_full_size_prefill_sampled(lib):
+def test_full_size_mtp_every_element(lib):
+    w = wl.by_name("mtp_b64_h16_q4_ps64")
+    out, lse = run_gpu(lib, w)
+    ref_out, ref_lse = oracle_run(w)
+    assert_close(out, lse, ref_out, ref_lse, "mtp_b64_h16_q4_ps64")
+
+
+def worker_boundary_rows(w, workers, row_cost=5, tile=64):
+    """Query rows in which a split-KV worker's range starts or ends, for a partition of
+    the cost sequence (a row start counts row_cost units, a 64-key tile one unit) into
+    ``workers`` even parts.  Used only to choose which rows to check."""
+    qo = w.qo_indptr.tolist()
+    kp = w.kv_indptr.tolist()
+    spans = []  # (first cost unit, last cost unit, row)
+    c = 0
+    for b in range(w.batch):
+        ql, kl = qo[b + 1] - qo[b], kp[b + 1] - kp[b]
+        for i in range(ql):
+            vis = kl - ql + i + 1
+            if vis <= 0:
+                continue
+            n = row_cost + -(-vis // tile)
+            spans.append((c, c + n - 1, qo[b] + i))
+            c += n
+    bounds = sorted({k * c // workers for k in range(1, workers)})
+    rows, j = set(), 0
+    for x in bounds:
+        while spans[j][1] < x:
+            j += 1
+        rows.add(spans[j][2])
+        if j > 0:
+            rows.add(spans[j - 1][2])
+    return rows
+
+
+def test_full_size_prefill_dense_rows(lib):
     w = wl.prefill_causal_h128()
     out, lse = run_gpu(lib, w)
-    qo = w.qo_indptr.tolist()
-    extra = [qo[b] for b in range(4)] + [qo[b + 1] - 1 for b in range(4)] + [qo[b] + 63 for b in range(4)] \
-        + [qo[b] + 64 for b in range(4)]
-    rows = _sample_rows(w.rows, extra=extra)
-    ref = oracle_rows_prefill(w, rows)
-    for r in rows:
-        assert_close(out[r], lse[r], ref[r][0], ref[r][1], f"prefill row {r}")
+    qo, kp = w.qo_indptr.tolist(), w.kv_indptr.tolist()
+    rows = set(range(0, w.rows, 8))
+    for b in range(w.batch):
+        ql, kl = qo[b + 1] - qo[b], kp[b + 1] - kp[b]
+        rows.update((qo[b], qo[b + 1] - 1))
+        for i in range(ql):
+            if (kl - ql + i + 1) % 64 in (0, 1):
+                rows.add(qo[b] + i)
+    rows |= worker_boundary_rows(w, lib.default_num_workers())
+    rows = sorted(rows)
+    ref_out, ref_lse = oracle_run(w, rows=rows)
+    assert_close(out[rows], lse[rows], ref_out[rows], ref_lse[rows], f"prefill_causal_h128 ({len(rows)} rows)")
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
