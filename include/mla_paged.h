@@ -188,6 +188,17 @@ const char* mla_status_string(int status);
  * Returns MLA_ERR_CUDA if the synchronisation itself reports an error. */
 int mla_read_device_status(void* workspace, void* stream);
 
+/* Test hook of the kernels' bounded waits (off by default; not for production use).
+ * With skip_tile >= 1, the attention kernel's producer for split-KV worker 0 (first CTA
+ * of the pair) skips the loads and the arrival of that tile of its range in every call
+ * that follows, so the waits on it run out; wait_ns sets the limit of every bounded wait
+ * (0 = the default of 4 s).  The kernel then gives up, unwinds (drains its copies and
+ * matrix operations, frees tensor memory) and records MLA_ERR_TIMEOUT in the status
+ * word, where mla_read_device_status finds it; outputs of that call are undefined.
+ * skip_tile = -1 restores normal calls.  Returns MLA_ERR_DIMS for skip_tile 0 or < -1.
+ * Not thread-safe with respect to calls in flight on other threads. */
+int mla_debug_inject_timeout(int skip_tile, unsigned long long wait_ns);
+
 /* Kernel timing for benchmarks.  When enabled, every call records CUDA events on its
  * stream around its main attention kernel and its combine kernel;
  * mla_profile_read synchronises on the last events, returns the summed milliseconds

@@ -60,6 +60,7 @@ _SIGNATURES = [
     ("mla_status_string", ctypes.c_char_p, [ctypes.c_int]),
     ("mla_read_device_status", ctypes.c_int, [_P, _P]),
     ("mla_noalloc_read_status", ctypes.c_int, [_P]),
+    ("mla_debug_inject_timeout", ctypes.c_int, [ctypes.c_int, ctypes.c_ulonglong]),
     ("mla_profile_enable", ctypes.c_int, [ctypes.c_int]),
     ("mla_profile_read", ctypes.c_int, [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                                         ctypes.POINTER(ctypes.c_int)]),

@@ -46,6 +46,11 @@ struct MlaParams {
   // kv_len - mtp_q + i + 1 keys (causal within the request).
   int mtp_q;
   int mtp_h;
+  // Bounded waits give up after wait_ns nanoseconds.  fault_skip_tile >= 1 makes the
+  // producer of worker 0, rank 0, skip that tile's loads and arrival (a test of the
+  // give-up path; -1 in normal calls).
+  unsigned long long wait_ns;
+  int fault_skip_tile;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

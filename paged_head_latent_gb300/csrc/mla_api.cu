@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -31,6 +32,11 @@ struct DeviceInfo {
 
 std::mutex g_mu;
 DeviceInfo g_dev[64];
+
+// Test hook of the bounded waits (mla_debug_inject_timeout): the wait limit and the
+// tile whose arrival worker 0's producer skips (-1: none).
+std::atomic<unsigned long long> g_wait_ns{4000000000ull};
+std::atomic<int> g_fault_skip_tile{-1};
 
 int query_device(DeviceInfo* out) {
   int dev = 0;
@@ -235,6 +241,8 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   p.num_kv_indices = p.num_slots > 0 ? dims->num_kv_indices : 0;
   p.workers = G;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
+  p.wait_ns = g_wait_ns.load();
+  p.fault_skip_tile = g_fault_skip_tile.load();
   unsigned char* ws = static_cast<unsigned char*>(workspace);
   p.status = reinterpret_cast<uint32_t*>(ws);
   p.records = reinterpret_cast<mla::CombineRecord*>(ws + lay.records);
@@ -350,6 +358,13 @@ int mla_read_device_status(void* workspace, void* stream_ptr) {
   if (word & mla::kStatusInternal) return MLA_ERR_INTERNAL;
   if (word & mla::kStatusTimeout) return MLA_ERR_TIMEOUT;
   if (word & mla::kStatusBadIndex) return MLA_ERR_BAD_INDEX;
+  return MLA_OK;
+}
+
+int mla_debug_inject_timeout(int skip_tile, unsigned long long wait_ns) {
+  if (skip_tile == 0 || skip_tile < -1) return MLA_ERR_DIMS;
+  g_wait_ns.store(wait_ns ? wait_ns : 4000000000ull);
+  g_fault_skip_tile.store(skip_tile);
   return MLA_OK;
 }
 

@@ -104,6 +104,18 @@ enum Bar : uint32_t {
   X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, DESC0, NUM_BARS
 };
 
+// The two softmax warps that serve the same TMEM lanes (w and w + 4) meet at a named
+// barrier.  A warp leaves the softmax loop early only after some wait gave up, which
+// raises the abort flag first; on leaving it arrives once at its pair barrier, which
+// releases a partner waiting there, and every warp reads the flag right after each
+// pair barrier and leaves too, so no warp waits at a pair barrier for ever.
+__device__ __forceinline__ void pair_sync(int warp) {
+  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+}
+__device__ __forceinline__ void pair_release(int warp) {
+  asm volatile("bar.arrive %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
+}
+
 struct Misc {
   uint32_t tmem;
   int abort;
@@ -142,10 +154,6 @@ __device__ __forceinline__ void unpack24(const uint32_t* w, float* x) {  // w[3]
 // conflicts.
 __device__ __forceinline__ uint32_t stg_slot(int r, int c) { return 16u * (4 * r + (c ^ ((r >> 1) & 3))); }
 
-__device__ __forceinline__ void pair_sync(int warp) {
-  // The two softmax warps that serve the same TMEM lanes (w and w + 4).
-  asm volatile("bar.sync %0, 64;" ::"r"(1 + (warp & 3)) : "memory");
-}
 
 // Tiles of a worker in order, with their segment.
 struct TileIter {
@@ -212,6 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile int* abort = &misc.abort;
+  const unsigned long long wait_ns = p.wait_ns;  // limit of every bounded wait
   auto bar = [&](uint32_t i) { return sbase + kOffBar + 8u * i; };
 
   if (threadIdx.x == 0) {
@@ -306,6 +315,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
     TileIter it;
     it.init(pa, cur);
     TileDesc* desc = reinterpret_cast<TileDesc*>(smem + kOffDesc);
+    const bool fault_worker = p.fault_skip_tile >= 1 && w == 0 && rank == 0;
     uint32_t j = 0;
     bool have_next = false;  // next_s0/next_s1 hold this tile's ids, loaded a tile ago
     int next_s0 = 0, next_s1 = 0;
@@ -323,10 +333,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         tile_slots(it.seg, it.t, s0, s1, contiguous, first);
       }
       if (j >= kStages &&
-          !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout))
+          !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout, wait_ns))
         break;
       const uint32_t kvbar = bar(KV_FULL0 + stage);
       const uint32_t dst = sbase + kOffKV + stage * kStageBytes;
+      const bool skip = fault_worker && (int)j == p.fault_skip_tile;
       if (lane == 0 && part == 0) {
         TileDesc d;
         d.t = it.t;
@@ -353,10 +364,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         if (j == 0) mbar_arrive(bar(DESC0));  // lets the softmax warps load Q early
         // TMA tile: the one arrival, with the tile's bytes (release: orders the descriptor
         // before the tile).  Copied tile: lane 0 arrives after the lanes' copies below.
-        if (contiguous) mbar_arrive_expect_tx(kvbar, kStageBytes);
+        if (contiguous && !skip) mbar_arrive_expect_tx(kvbar, kStageBytes);
       }
       __syncwarp();
-      if (contiguous) {
+      if (skip) {
+        // Test of the give-up path: this tile is never loaded and never arrives, so every
+        // wait on it runs into its limit.
+      } else if (contiguous) {
         if (kGather && part == 1) {
           if (lane == 0) mbar_arrive(kvbar);
         } else if (lane == 0) {
@@ -433,7 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       volatile int no_abort = 0;
       for (uint32_t s = 0; s < kStages && s < j; ++s) {
         const uint32_t last = j - 1 - ((j - 1 - s) % kStages);
-        mbar_wait(bar(KV_FULL0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout);
+        if (fault_worker && (int)last == p.fault_skip_tile) continue;  // never issued
+        mbar_wait(bar(KV_FULL0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout, wait_ns);
       }
     }
   } else if (warp == kMmaWarp || warp == kPvWarp) {
@@ -450,10 +465,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         // S = Q . K^T for every tile (TS form: Q slice in TMEM, K tile in shared memory).
         for (uint32_t jq = 0; jq < ntiles; ++jq) {
           const uint32_t stage = jq % kStages;
-          if (!mbar_wait(bar(KV_FULL0 + stage), (jq / kStages) & 1, abort, p.status, kStatusTimeout)) break;
+          if (!mbar_wait(bar(KV_FULL0 + stage), (jq / kStages) & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
           const TileDesc d = desc[jq % kDescRing];
-          if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout)) ||
-              (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout)))
+          if (((d.flags & kFirst) && !mbar_wait(bar(Q_FULL), d.nseg & 1, abort, p.status, kStatusTimeout, wait_ns)) ||
+              (jq >= 1 && !mbar_wait(bar(S_EMPTY), (jq - 1) & 1, abort, p.status, kStatusTimeout, wait_ns)))
             break;
           if (d.flags & kCopied) fence_proxy_async_smem();  // written through the generic proxy
           tc_fence_after();
@@ -478,10 +493,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         // tile's KV_FULL and only then arrive on P_FULL.
         for (uint32_t jv = 0; jv < ntiles; ++jv) {
           const uint32_t stage = jv % kStages;
-          if (!mbar_wait(bar(P_FULL), jv & 1, abort, p.status, kStatusTimeout)) break;
+          if (!mbar_wait(bar(P_FULL), jv & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
           const TileDesc d = desc[jv % kDescRing];
           const bool first = d.flags & kFirst;
-          if (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout))
+          if (first && d.nseg > 0 && !mbar_wait(bar(O_EMPTY), (d.nseg - 1) & 1, abort, p.status, kStatusTimeout, wait_ns))
             break;
           if (d.flags & kCopied) fence_proxy_async_smem();  // written through the generic proxy
           tc_fence_after();
@@ -500,7 +515,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       // one commit from each of the two issuing threads).
       mma_commit(bar(DRAIN));
       volatile int no_abort = 0;
-      mbar_wait(bar(DRAIN), 0, &no_abort, p.status, kStatusTimeout);
+      mbar_wait(bar(DRAIN), 0, &no_abort, p.status, kStatusTimeout, wait_ns);
     }
     __syncwarp();
   } else {
@@ -611,14 +626,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
     // after this tile's piece has left for the peer, off the exchange's critical path).
     int q_pending = -1;
     auto fetch = [&]() -> bool {
-      if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout)) return false;
+      if (!mbar_wait(bar(S_FULL), jf & 1, abort, p.status, kStatusTimeout, wait_ns)) return false;
       tc_fence_after();
       uint32_t sn[32];
       tmem_ld32(tmem + lane_base + kColS + 32 * half, sn);
       // The tile's descriptor: its KV_FULL phase has completed (QK read the tile); the
       // barrier probe overlaps the TMEM load.
       const bool kv_ok =
-          mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout);
+          mbar_wait(bar(KV_FULL0 + jf % kStages), (jf / kStages) & 1, abort, p.status, kStatusTimeout, wait_ns);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -648,7 +663,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         st_async_v4(dst + c * 512, v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3], xfull_remote + 64 * (t & 1));
     };
     if (ntiles > 0) {
-      if (!mbar_wait(bar(DESC0), 0, abort, p.status, kStatusTimeout)) {
+      if (!mbar_wait(bar(DESC0), 0, abort, p.status, kStatusTimeout, wait_ns)) {
         ok = false;
       } else {
         write_q(desc[0].row);
@@ -673,7 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       // Tile j+1's partial is fetched before this warp waits for tile j's piece, so it
       // can leave the moment tile j's has arrived.
       if (jf < ntiles && !fetch()) break;
-      if (!mbar_wait<true>(bar(X_FULL0 + 8 * b + warp), (j >> 1) & 1, abort, p.status, kStatusTimeout)) break;
+      if (!mbar_wait<true>(bar(X_FULL0 + 8 * b + warp), (j >> 1) & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
       // The peer's piece of tile j is here: load it, then send tile j+1 at once (the send
       // is what the peer waits for, so the unpacking below stays off that path).  The
       // loads are issued before the stores; the buffer is rewritten only with the peer's
@@ -721,6 +736,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       if (full) mx *= scale;
       red[(b * 2 + half) * 128 + row] = mx;
       pair_sync(warp);
+      if (*abort) break;
       mx = fmaxf(mx, red[(b * 2 + (half ^ 1)) * 128 + row]);
       float alpha = 1.f;
       bool rescale = false;
@@ -758,7 +774,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
       l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       // P is single-buffered: the previous tile's P.V must be done (it also settles O).
-      if (j >= 1 && !mbar_wait(bar(PV_DONE), (j - 1) & 1, abort, p.status, kStatusTimeout)) break;
+      if (j >= 1 && !mbar_wait(bar(PV_DONE), (j - 1) & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
       tc_fence_after();
       if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
@@ -782,8 +798,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         // Epilogue: O / l to out (whole rows) or to the workspace (split rows).
         lbuf[half * 128 + row] = l;
         pair_sync(warp);
+        if (*abort) break;
         const float lt = l + lbuf[(half ^ 1) * 128 + row];
-        if (!mbar_wait(bar(O_FULL), cd.nseg & 1, abort, p.status, kStatusTimeout)) break;
+        if (!mbar_wait(bar(O_FULL), cd.nseg & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
         tc_fence_after();
         const float inv_l = (kPack && !(lt > 0.f)) ? 0.f : 1.f / lt;  // (no key: out 0, lse -inf)
         const float lse2 = m_ref + fast_log2(lt);
@@ -840,6 +857,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
       ++j;
     }
+    // Every tile processed, or the loop left early (only ever after the abort flag was
+    // raised): then release the partner, which may be waiting at the pair barrier.
+    if (!ok || j < ntiles) pair_release(warp);
   }
 
   // The merge kernel, launched with programmatic stream serialisation, may be

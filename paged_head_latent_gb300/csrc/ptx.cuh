@@ -8,7 +8,7 @@
 namespace mla {
 namespace ptx {
 
-constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s
+constexpr unsigned long long kWaitTimeoutNs = 4000000000ull;  // 4 s (the default limit)
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -79,19 +79,20 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Wait for the phase with parity `parity` to complete.  Gives up after
-// kWaitTimeoutNs, or as soon as another role raised *abort; on giving up it sets
+// Wait for the phase with parity `parity` to complete.  Gives up after limit_ns
+// nanoseconds, or as soon as another role raised *abort; on giving up it sets
 // `timeout_bit` in *status, raises *abort and returns false.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                          uint32_t* status, uint32_t timeout_bit) {
+                                          uint32_t* status, uint32_t timeout_bit,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
   if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
+      if (globaltimer() - t0 > limit_ns) {
         atomicOr(status, timeout_bit);
         *abort = 1;
         return false;
