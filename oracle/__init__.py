@@ -5,8 +5,8 @@ may import this package.  It shares no code with the CUDA path.
 """
 
 from .mla_oracle import (attend, combine_partials, mla_decode, mla_decode_split, mla_prefill,
-                         online_softmax_partial, scores, visible_len)
+                         mla_sparse_decode, online_softmax_partial, scores, visible_len)
 from .brute import brute_decode, brute_prefill
 
-__all__ = ["attend", "combine_partials", "mla_decode", "mla_decode_split", "mla_prefill",
+__all__ = ["attend", "combine_partials", "mla_decode", "mla_decode_split", "mla_prefill", "mla_sparse_decode",
            "online_softmax_partial", "scores", "visible_len", "brute_decode", "brute_prefill"]

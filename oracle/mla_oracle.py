@@ -152,6 +152,33 @@ def mla_prefill(q_nope, q_pe, ckv_cache, kpe_cache, qo_indptr, kv_indptr, kv_ind
     return out, lse
 
 
+def mla_sparse_decode(q_nope, q_pe, ckv_cache, kpe_cache, indices, sm_scale):
+    """Sparse (top-k) MLA decode (FlashMLA notes, "flash_mla_with_kvcache (Sparse
+    Attention with FP8 KV Cache)" and "Sparse Attention Decoding with KV Cache": each
+    query attends only to the token slots listed for it; "Sparse MLA Prefill Kernel":
+    invalid entries are -1 or any value >= the number of tokens).
+
+    q_nope [R, H, 512], q_pe [R, H, 64] -- one row per (request, query token); indices
+    [R, topk] token slots into the caches viewed as [num_slots, 512] / [.., 64].  Entries
+    outside [0, num_slots) are padding and skipped; a slot listed twice counts twice.
+    No causal mask.  Returns output [R, H, 512] and lse [R, H] (natural log); a row
+    without a valid entry gets 0 and -inf.
+    """
+    ckv, kpe = _flat_caches(ckv_cache, kpe_cache)
+    n = ckv.shape[0]
+    idx = np.asarray(indices, dtype=np.int64)
+    q_nope = np.asarray(q_nope)
+    q_pe = np.asarray(q_pe)
+    r_count, h = q_nope.shape[0], q_nope.shape[1]
+    out = np.zeros((r_count, h, HEAD_DIM_CKV))
+    lse = np.zeros((r_count, h))
+    for r in range(r_count):
+        sel = idx[r]
+        sel = sel[(sel >= 0) & (sel < n)]
+        out[r], lse[r] = attend(q_nope[r], q_pe[r], ckv[sel], kpe[sel], sm_scale)
+    return out, lse
+
+
 # ---------------------------------------------------------------------------
 # Split-KV form: blocked online softmax per split, then the partial combine.
 # ---------------------------------------------------------------------------

@@ -53,6 +53,10 @@ class Workload:
     kv_indptr: torch.Tensor
     kv_indices: torch.Tensor
     qo_indptr: Optional[torch.Tensor] = None
+    # Sparse (top-k) decode: [rows, topk] token slots per query row; entries outside the
+    # cache are padding.  kv_indptr / kv_indices then hold the same lists as a CSR view
+    # (row r owns entries r*topk .. r*topk + topk - 1).
+    indices: Optional[torch.Tensor] = None
 
     @property
     def batch(self) -> int:
@@ -72,6 +76,15 @@ class Workload:
     def num_kv_indices(self) -> int:
         return self.kv_indices.numel()
 
+    @property
+    def topk(self) -> int:
+        return self.indices.shape[1] if self.indices is not None else 0
+
+    def valid_per_row(self) -> List[int]:
+        """Sparse decode: entries of each row that name a slot of the cache."""
+        n = self.num_pages * self.page_size
+        return ((self.indices >= 0) & (self.indices < n)).sum(dim=1).tolist()
+
     def kv_lens(self) -> List[int]:
         p = self.kv_indptr.tolist()
         return [p[i + 1] - p[i] for i in range(len(p) - 1)]
@@ -86,6 +99,8 @@ class Workload:
         """Number of (query row, key) pairs the operator scores, per head."""
         if self.kind == "decode":
             return sum(self.kv_lens())
+        if self.kind == "sparse":
+            return sum(self.valid_per_row())
         total = 0
         for ql, kl in zip(self.q_lens(), self.kv_lens()):
             prefix = kl - ql
@@ -98,6 +113,8 @@ class Workload:
                  kv_indices=self.kv_indices)
         if self.qo_indptr is not None:
             d["qo_indptr"] = self.qo_indptr
+        if self.indices is not None:
+            d["indices"] = self.indices
         return d
 
     def to(self, device) -> "Workload":
@@ -210,12 +227,47 @@ def make_mtp(kv_lens: Optional[Sequence[int]], q_len: int, num_qo_heads: int, pa
     return dataclasses.replace(w, kind="mtp")
 
 
+def make_sparse_decode(kv_lens: Optional[Sequence[int]], topk: int, num_qo_heads: int, page_size: int,
+                       seed: int, s_q: int = 1, kv_lens_fn=None, name: str = "sparse") -> Workload:
+    """Sparse (top-k) decode: each of a request's s_q query tokens attends to its own
+    list of topk token slots of that request (FlashMLA's sparse decoding, where an
+    indexer picks the keys).  Slots are drawn without replacement from the request's
+    slots in random order; a request with fewer than topk keys lists all of them and
+    pads with -1.  Draw order: kv lengths, page permutation, index draws (row by row),
+    q_nope, q_pe, ckv_cache, kpe_cache."""
+    gen = torch.Generator().manual_seed(seed)
+    if kv_lens_fn is not None:
+        kv_lens = kv_lens_fn(gen)
+    kv_lens = [int(x) for x in kv_lens]
+    indptr, slots, num_pages = _page_table(kv_lens, page_size, None, gen, False)
+    ip = indptr.tolist()
+    rows = []
+    for b, l in enumerate(kv_lens):
+        own = slots[ip[b]:ip[b + 1]]
+        for _ in range(s_q):
+            take = min(topk, l)
+            pick = own[torch.randperm(l, generator=gen)[:take]] if take else own[:0]
+            rows.append(torch.cat([pick, torch.full((topk - take,), -1, dtype=torch.int32)]))
+    indices = torch.stack(rows).to(torch.int32).contiguous()
+    r = len(rows)
+    q_nope = _randn_bf16((r, num_qo_heads, HEAD_DIM_CKV), gen)
+    q_pe = _randn_bf16((r, num_qo_heads, HEAD_DIM_KPE), gen)
+    ckv = _randn_bf16((num_pages, page_size, HEAD_DIM_CKV), gen)
+    kpe = _randn_bf16((num_pages, page_size, HEAD_DIM_KPE), gen)
+    csr_indptr = torch.arange(r + 1, dtype=torch.int32) * topk
+    return Workload(name=name, kind="sparse", num_qo_heads=num_qo_heads, page_size=page_size,
+                    num_pages=num_pages, sm_scale=DEFAULT_SM_SCALE, q_nope=q_nope, q_pe=q_pe,
+                    ckv_cache=ckv, kpe_cache=kpe, kv_indptr=csr_indptr, kv_indices=indices.reshape(-1).clone(),
+                    indices=indices)
+
+
 def poison_unreferenced(w: Workload, value: float = float("nan")) -> Workload:
     """Return a copy whose cache slots not named in kv_indices hold ``value``."""
     ckv = w.ckv_cache.clone()
     kpe = w.kpe_cache.clone()
     used = torch.zeros(w.num_pages * w.page_size, dtype=torch.bool)
-    used[w.kv_indices.long()] = True
+    idx = w.kv_indices.long()
+    used[idx[(idx >= 0) & (idx < used.numel())]] = True
     ckv.view(-1, HEAD_DIM_CKV)[~used] = value
     kpe.view(-1, HEAD_DIM_KPE)[~used] = value
     return dataclasses.replace(w, ckv_cache=ckv, kpe_cache=kpe)
@@ -266,6 +318,18 @@ def mtp_b64_h16_q4_ps64() -> Workload:
                     name="mtp_b64_h16_q4_ps64")
 
 
+def sparse_b64_h128_topk2048() -> Workload:
+    """Sparse decode: 64 requests of 128 heads, page 64; 60 requests of 4096..16384 keys
+    and 4 of 512..2047 keys (shorter than topk, so padded with -1); each query attends to
+    2048 of its request's keys."""
+    def lens(gen):
+        long = torch.randint(4096, 16385, (60,), generator=gen).tolist()
+        short = torch.randint(512, 2048, (4,), generator=gen).tolist()
+        return long[:15] + short[:1] + long[15:30] + short[1:2] + long[30:45] + short[2:3] + long[45:] + short[3:]
+    return make_sparse_decode(None, 2048, num_qo_heads=128, page_size=64, seed=1007, kv_lens_fn=lens,
+                              name="sparse_b64_h128_topk2048")
+
+
 NAMED = {
     "decode_b4_h16_ps64": decode_b4_h16_ps64,
     "decode_b64_h128_ps64": decode_b64_h128_ps64,
@@ -273,6 +337,7 @@ NAMED = {
     "decode_b32_h128_skew": decode_b32_h128_skew,
     "prefill_causal_h128": prefill_causal_h128,
     "mtp_b64_h16_q4_ps64": mtp_b64_h16_q4_ps64,
+    "sparse_b64_h128_topk2048": sparse_b64_h128_topk2048,
 }
 
 

@@ -20,12 +20,17 @@ def np_inputs(w):
     )
     if w.qo_indptr is not None:
         d["qo_indptr"] = w.qo_indptr.numpy().astype(np.int64)
+    if w.indices is not None:
+        d["indices"] = w.indices.numpy().astype(np.int64)
     return d
 
 
 def oracle_run(w, rows=None):
     import oracle
     a = np_inputs(w)
+    if w.kind == "sparse":
+        return oracle.mla_sparse_decode(a["q_nope"], a["q_pe"], a["ckv_cache"], a["kpe_cache"], a["indices"],
+                                        a["sm_scale"])
     if w.kind == "decode":
         out, lse = oracle.mla_decode(a["q_nope"], a["q_pe"], a["ckv_cache"], a["kpe_cache"],
                                      a["kv_indptr"], a["kv_indices"], a["sm_scale"])
