@@ -9,7 +9,8 @@ launching stream.  ``value`` is the median microseconds per call of the headline
 workload (decode, batch 128, 128 heads, page size 1, 4096 keys each: the largest
 single-GPU decode configuration); p10/p90 and the mean are reported beside it.
 ``configs`` holds the same measurements for the other named workloads (the small
-decode, the page-64 decode, the skewed decode, the causal prefill).  ``e2e`` times the
+decode, the page-64 decode, the skewed decode, the causal prefill, the packed
+multi-token decode and the sparse top-k decode).  ``e2e`` times the
 headline call from pinned host buffers: host->device copies of every input, the call,
 and the device->host copy of out and lse.
 
@@ -34,7 +35,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA paged decode µs/call, KV TB/s & TFLOP/s as % of GB300 roofline"
 HEADLINE = "decode_b128_h128_ps1"
-SUB_WORKLOADS = ("decode_b4_h16_ps64", "decode_b64_h128_ps64", "decode_b32_h128_skew", "prefill_causal_h128")
+SUB_WORKLOADS = ("decode_b4_h16_ps64", "decode_b64_h128_ps64", "decode_b32_h128_skew", "prefill_causal_h128",
+                 "mtp_b64_h16_q4_ps64", "sparse_b64_h128_topk2048")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -53,10 +55,14 @@ def algorithmic_work(w):
     1152 B + 4 B index per cached key of a request (a prefill request's query rows share
     its keys, so each is read once); 1152 B q + 1024 B out + 4 B lse per (row, head);
     2 * (576 + 512) flops per (visible key, head), a visible key being a (query row, key)
-    pair that the causal mask keeps."""
+    pair that the causal mask keeps.  Sparse decode: 1152 B per valid entry (padding
+    entries read only their 4 B index)."""
     keys = w.visible_keys()
     rows_heads = w.rows * w.num_qo_heads
-    nbytes = sum(w.kv_lens()) * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
+    if w.kind == "sparse":
+        nbytes = keys * 1152 + w.num_kv_indices * 4 + rows_heads * (1152 + 1024 + 4)
+    else:
+        nbytes = sum(w.kv_lens()) * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
     flops = keys * w.num_qo_heads * 2 * (576 + 512)
     return nbytes, flops, keys
 
@@ -179,9 +185,10 @@ def time_oracle(w, budget_s, max_rows=None):
     for k in order:
         r, k0, n = rows[k]
         slots = w.kv_indices[k0:k0 + max(n, 0)].long()
+        slots = slots[(slots >= 0) & (slots < ckv.shape[0])]  # sparse decode: padding entries are skipped
         oracle.attend(w.q_nope[r].float().numpy(), w.q_pe[r].float().numpy(), ckv[slots].float().numpy(),
                       kpe[slots].float().numpy(), w.sm_scale)
-        keys += max(n, 0)
+        keys += slots.numel()
         done += 1
         if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):
             break

@@ -30,8 +30,8 @@
  *    they may be captured in a CUDA graph.  Launch errors are returned; faults
  *    inside a kernel surface at the caller's next synchronisation.
  *  - Slots outside kv_indices are never read into the result: NaN or Inf there does
- *    not change the output.  An index outside [0, num_pages*page_size) reads zeros
- *    (TMA out-of-bounds fill) instead of faulting; MLA_VALIDATE reports it.
+ *    not change the output.  An index outside [0, num_pages*page_size) is skipped (it
+ *    is not a key of the row) instead of faulting; MLA_VALIDATE reports it.
  *  - A request with no keys gets out = 0 and lse = -inf.
  */
 #ifndef MLA_PAGED_H
@@ -137,6 +137,26 @@ int mla_paged_decode_mtp(const void* q_nope, const void* q_pe, const void* ckv_c
                          const void* kpe_cache, const int32_t* kv_indptr, const int32_t* kv_indices,
                          float sm_scale, void* out, float* lse, const mla_dims* dims, int q_len,
                          void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
+ * Sparse (top-k) paged MLA decode: FlashMLA notes, "flash_mla_with_kvcache (Sparse
+ * Attention with FP8 KV Cache)" and "Sparse Attention Decoding with KV Cache" (bf16
+ * caches here).  Every query row attends only to the token slots listed for it, with no
+ * causal mask.
+ *   q_nope [rows, H, 512], q_pe [rows, H, 64] bf16: one row per (request, query token),
+ *          e.g. [batch, s_q, H, 512] viewed as [batch * s_q, H, 512]
+ *   indices [rows, topk] int32 token slots (slot = page * page_size + offset); an entry
+ *          that is negative or >= num_pages * page_size is padding and is skipped; a
+ *          row without a valid entry gets out = 0, lse = -inf
+ *   out [rows, H, 512] bf16, lse [rows, H] fp32 (natural log)
+ *   dims->batch = rows; dims->num_kv_indices is ignored (rows * topk); other fields as
+ *   for mla_paged_decode; workspace >= mla_workspace_bytes(dims, 0).  MLA_VALIDATE
+ *   checks nothing here (any index may be padding).
+ */
+int mla_paged_decode_sparse(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const void* kpe_cache, const int32_t* indices, int topk, float sm_scale,
+                            void* out, float* lse, const mla_dims* dims, void* workspace,
+                            size_t workspace_bytes, int flags, void* stream);
 
 /*
  * Paged MLA decode for callers that cannot allocate device memory (a plugin that runs

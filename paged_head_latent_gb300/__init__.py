@@ -52,6 +52,9 @@ _SIGNATURES = [
     ("mla_paged_decode_mtp", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P,
       ctypes.c_size_t, ctypes.c_int, _P]),
+    ("mla_paged_decode_sparse", ctypes.c_int,
+     [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
+      ctypes.c_int, _P]),
     ("mla_paged_decode_noalloc", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P]),
     ("mla_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
@@ -263,6 +266,49 @@ def mla_paged_decode_mtp(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indic
     return out, lse
 
 
+def mla_paged_decode_sparse(q_nope, q_pe, ckv_cache, kpe_cache, indices, sm_scale, out=None, lse=None,
+                            workspace=None, flags=0, num_workers=0,
+                            stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse (top-k) decode: row r of q attends to the token slots indices[r, :]
+    (entries outside the cache are padding).  q_nope [rows, H, 512], q_pe [rows, H, 64],
+    indices [rows, topk] int32.  Returns (out [rows, H, 512], lse [rows, H])."""
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache), ("kpe_cache", kpe_cache)):
+        _check_cuda(n, t, torch.bfloat16)
+    _check_cuda("indices", indices, torch.int32)
+    rows, heads = q_nope.shape[0], q_nope.shape[1]
+    if q_nope.shape != (rows, heads, HEAD_DIM_CKV) or q_pe.shape != (rows, heads, HEAD_DIM_KPE):
+        raise ValueError("q_nope must be [rows, H, 512] and q_pe [rows, H, 64]")
+    if indices.dim() != 2 or indices.shape[0] != rows:
+        raise ValueError("indices must be [rows, topk]")
+    topk = indices.shape[1]
+    num_pages, page_size = _cache_geometry(ckv_cache, kpe_cache)
+    dims = make_dims(rows, heads, num_pages, page_size, rows * topk, num_workers=num_workers)
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty(rows, heads, HEAD_DIM_CKV, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=dev)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("lse", lse, torch.float32)
+    if out.shape != (rows, heads, HEAD_DIM_CKV) or lse.shape != (rows, heads):
+        raise ValueError("out must be [rows, H, 512] and lse [rows, H]")
+    need = workspace_bytes(dims, False)
+    if need == 0:
+        raise MlaError(-2, "mla_workspace_bytes")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = lib().mla_paged_decode_sparse(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                           _ptr(indices), int(topk), float(sm_scale), _ptr(out), _ptr(lse),
+                                           ctypes.byref(dims), _ptr(workspace), workspace.numel(), int(flags),
+                                           ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise MlaError(st, "mla_paged_decode_sparse")
+    return out, lse
+
+
 def mla_paged_decode_noalloc(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_scale,
                              out, lse, num_workers=0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
     """Paged MLA decode without a workspace argument, for callers that cannot allocate
@@ -331,8 +377,14 @@ def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
                  stream=stream)  # validates everything once
     dims = workload_dims(w, num_workers)
     sp = ctypes.c_void_p(stream.cuda_stream)
-    name = {"decode": "mla_paged_decode", "prefill": "mla_paged_prefill", "mtp": "mla_paged_decode_mtp"}[w.kind]
-    if w.kind == "mtp":
+    name = {"decode": "mla_paged_decode", "prefill": "mla_paged_prefill", "mtp": "mla_paged_decode_mtp",
+            "sparse": "mla_paged_decode_sparse"}[w.kind]
+    if w.kind == "sparse":
+        fn = lib().mla_paged_decode_sparse
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.indices),
+                int(w.topk), float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
+                workspace.numel(), int(flags), sp)
+    elif w.kind == "mtp":
         fn = lib().mla_paged_decode_mtp
         args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.kv_indptr),
                 _ptr(w.kv_indices), float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
@@ -359,7 +411,7 @@ def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
 
 
 def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, stream=None):
-    """Call decode, prefill or packed multi-token decode on a ``workloads.Workload`` whose
+    """Call decode, prefill, packed multi-token or sparse decode on a ``workloads.Workload`` whose
     tensors are on the GPU.  Returns (out, lse) shaped [rows, H, 512] and [rows, H]."""
     if w.kind == "mtp":
         b, q, h = w.batch, w.mtp_q_len, w.num_qo_heads
@@ -369,6 +421,9 @@ def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, 
                                       w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
                                       o4, l3, workspace, flags, num_workers, stream)
         return o4.view(b * q, h, HEAD_DIM_CKV), l3.view(b * q, h)
+    if w.kind == "sparse":
+        return mla_paged_decode_sparse(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.indices, w.sm_scale,
+                                       out, lse, workspace, flags, num_workers, stream)
     if w.kind == "decode":
         return mla_paged_decode(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices,
                                 w.sm_scale, out, lse, workspace, flags, num_workers, stream)

@@ -23,7 +23,7 @@ struct MlaParams {
   const __nv_bfloat16* q_pe;    // [rows, H, 64]
   const __nv_bfloat16* ckv;     // [num_slots, 512]
   const __nv_bfloat16* kpe;     // [num_slots, 64]
-  const int32_t* kv_indptr;     // [batch + 1]
+  const int32_t* kv_indptr;     // [batch + 1], or nullptr (sparse decode: topk entries per row)
   const int32_t* qo_indptr;     // [batch + 1] or nullptr (decode)
   const int32_t* kv_indices;    // [num_kv_indices]
   __nv_bfloat16* out;           // [rows, H, 512]
@@ -51,6 +51,7 @@ struct MlaParams {
   // give-up path; -1 in normal calls).
   unsigned long long wait_ns;
   int fault_skip_tile;
+  int topk;  // sparse decode: entries per row (kv_indptr is nullptr); 0 otherwise
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -87,7 +88,7 @@ namespace mla {
 // kv_len < q_len) get out = 0 and lse = -inf.  Run by one full warp of one CTA.
 __device__ inline void warp_write_empty_rows(const MlaParams& p) {
   const int lane = threadIdx.x & 31;
-  PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices};
+  PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices, p.topk};
   for (int base = 0; base < p.batch; base += 32) {
     int b = base + lane;
     int n_empty = 0, row0 = 0;

@@ -191,16 +191,19 @@ cudaEvent_t* profile_slot() {
 // multi-token decode (q_len > 0).
 int packed_heads(const mla_dims* d, int q_len) { return q_len > 0 ? q_len * d->num_qo_heads : d->num_qo_heads; }
 
+// topk > 0: sparse decode (kv_indptr unused; row b owns kv_indices[b*topk .. +topk)).
 int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const void* ckv_cache,
         const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
-        void* workspace, size_t workspace_bytes, int flags, void* stream_ptr) {
+        void* workspace, size_t workspace_bytes, int flags, void* stream_ptr, int topk = 0) {
   int st = check_dims(dims, prefill);
   if (st != MLA_OK) return st;
+  if (topk < 0) return MLA_ERR_DIMS;
+  if (topk > 0 && (long long)dims->batch * topk != dims->num_kv_indices) return MLA_ERR_DIMS;
   if (q_len < 0 || packed_heads(dims, q_len) > mla::kMaxHeads) return MLA_ERR_DIMS;
   if ((long long)dims->batch * packed_heads(dims, q_len) >= (1LL << 31)) return MLA_ERR_DIMS;
   const long long rows = prefill ? dims->total_q : dims->batch;
-  if (!q_nope || !q_pe || !kv_indptr || !out || !lse) return MLA_ERR_NULL;
+  if (!q_nope || !q_pe || (!kv_indptr && topk == 0) || !out || !lse) return MLA_ERR_NULL;
   // The caches may be NULL only when they hold no slot at all.
   if ((!ckv_cache || !kpe_cache) && dims->num_pages > 0) return MLA_ERR_NULL;
   if (prefill && !qo_indptr) return MLA_ERR_NULL;
@@ -226,7 +229,8 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   p.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
   p.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
-  p.kv_indptr = kv_indptr;
+  p.kv_indptr = topk > 0 ? nullptr : kv_indptr;
+  p.topk = topk;
   p.qo_indptr = prefill ? qo_indptr : nullptr;
   p.kv_indices = kv_indices;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -265,7 +269,10 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
     mla::TmaMaps maps;
     st = build_maps(p, &maps);
     if (st != MLA_OK) return st;
-    if (mla::launch_tc(maps, p, dims->page_size % 64 != 0, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
+    // Small pages, or the scattered keys of sparse decode: the instance that copies
+    // tiles slot by slot with two warps.
+    const bool gather = dims->page_size % 64 != 0 || topk > 0;
+    if (mla::launch_tc(maps, p, gather, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
   }
   if (ev) cudaEventRecord(ev[1], stream);
   if (mla::launch_combine(p, stream) != cudaSuccess) return MLA_ERR_LAUNCH;
@@ -292,6 +299,20 @@ int mla_paged_decode_mtp(const void* q_nope, const void* q_pe, const void* ckv_c
   if (q_len < 1) return MLA_ERR_DIMS;
   return run(false, q_len, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, kv_indptr, kv_indices, sm_scale,
              out, lse, dims, workspace, workspace_bytes, flags, stream);
+}
+
+int mla_paged_decode_sparse(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                            const void* kpe_cache, const int32_t* indices, int topk, float sm_scale,
+                            void* out, float* lse, const mla_dims* dims, void* workspace,
+                            size_t workspace_bytes, int flags, void* stream) {
+  if (!dims) return MLA_ERR_NULL;
+  if (topk < 1) return MLA_ERR_DIMS;
+  if ((long long)dims->batch * topk >= (1LL << 31)) return MLA_ERR_DIMS;
+  mla_dims d = *dims;
+  d.num_kv_indices = dims->batch * topk;
+  if (d.batch > 0 && !indices) return MLA_ERR_NULL;
+  return run(false, 0, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, nullptr, indices, sm_scale, out, lse, &d,
+             workspace, workspace_bytes, flags, stream, topk);
 }
 
 int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cache,

@@ -70,11 +70,14 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;    // issues S = Q.K^T; owns TMEM
 constexpr int kPvWarp = 10;    // issues O += P.V
-constexpr int kThreads = 352;
 // The small-page instance has a second copy warp: a copied tile's keys are split
 // between the two warps (32 each).
 constexpr int kCopyWarp2 = 11;
-constexpr int kThreadsGather = 384;
+// Threads of an instance.  The page-aligned instance without packed tokens has an idle
+// twelfth warp: with it the compiled softmax loop runs measurably faster (prefill ~8%),
+// while the packed-token instance is faster with eleven.
+template <bool kGather, bool kPack>
+constexpr int instance_threads() { return kGather || !kPack ? 384 : 352; }
 constexpr int kStages = 4;
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
@@ -89,7 +92,7 @@ constexpr uint32_t kOffL = kOffRed + 2 * 2 * 128 * 4;  // [2][128] row sums
 constexpr uint32_t kOffStg = kOffL + 2 * 128 * 4;  // [softmax warp] 2 KB: Q in / O out transposes
 constexpr uint32_t kOffDesc = kOffStg + 8 * 2048;  // ring of kDescRing tile descriptors
 constexpr int kDescRing = 8;
-constexpr uint32_t kOffBar = kOffDesc + kDescRing * 32;
+constexpr uint32_t kOffBar = kOffDesc + kDescRing * 40;
 constexpr uint32_t kOffMisc = kOffBar + 512;
 constexpr uint32_t kSmemBytes = kOffMisc + 64;
 constexpr uint32_t kTmemCols = 512;
@@ -190,17 +193,20 @@ struct TileIter {
 // rewritten only for tile j + kDescRing, i.e. after P.V of tile j + kDescRing - kStages,
 // by which time every reader of tile j is done with it.
 struct TileDesc {
-  int t;         // tile within the query row
-  int len;       // keys the row sees
-  int row;       // query row (decode: request)
-  int slot;      // partial-result slot of the segment
-  int nseg;      // index of the segment among this worker's segments
-  int flags;     // kFirst | kLast | kWhole | kCopied (loaded by cp.async, not TMA)
-  int next_row;  // query row of the next segment when kLast, else -1
+  int t;              // tile within the query row
+  int len;            // keys the row sees
+  int row;            // query row (decode: request)
+  int next_row;       // query row of the next segment when kLast, else -1
+  int slot;           // partial-result slot of the segment
+  int flags;          // kFirst | kLast | kWhole | kCopied (loaded by cp.async, not TMA)
+  int nseg;           // index of the segment among this worker's segments
   int pad;
+  // Bit k: key k of the tile is one of the row's keys and names a slot of the cache
+  // (keys past the row's length, padding entries and out-of-range slots are skipped).
+  unsigned long long valid;
 };
 constexpr int kFirst = 1, kLast = 2, kWhole = 4, kCopied = 8;
-static_assert(sizeof(TileDesc) == 32, "descriptor size");
+static_assert(sizeof(TileDesc) == 40, "descriptor size");
 
 }  // namespace
 
@@ -209,7 +215,7 @@ static_assert(sizeof(TileDesc) == 32, "descriptor size");
 // kPack: packed multi-token decode; TMEM lane m holds token m / mtp_h, head m % mtp_h of
 // the request, and each token's causal horizon masks the scores lane by lane.
 template <bool kGather, bool kPack>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGather : kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGather, kPack>(), 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -248,7 +254,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
     tmem_alloc(sbase + kOffMisc, kTmemCols);  // misc.tmem is the first word of Misc
     tmem_relinquish();
   }
-  const PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices};
+  const PlanArgs pa{p.kv_indptr, p.qo_indptr, p.batch, p.num_kv_indices, p.topk};
   if (warp == 0) {
     Cursor c;
     const long long C = warp_plan(pa, w, p.workers, &c);
@@ -294,19 +300,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
     // takes a few instructions, so its ids are loaded just before the wait for its stage;
     // with small pages (kGather) a copied tile's copies take long to issue, so the next
     // tile's ids (same row) are loaded before them and are ready when that tile comes up.
-    auto eval_slots = [&](int nvalid, int s0, int s1, bool& contiguous, int& first) {
+    auto eval_slots = [&](int nvalid, int s0, int s1, bool& contiguous, int& first, unsigned long long& valid) {
       first = __shfl_sync(0xffffffffu, s0, 0);
       const bool run = nvalid == kTileKeys && s0 == first + lane && s1 == first + lane + 32 && first >= 0 &&
                        first <= p.num_slots - kTileKeys;
       contiguous = __all_sync(0xffffffffu, run);
+      // Keys past the row's length carry slot num_slots, so the range test covers them.
+      const unsigned lo = __ballot_sync(0xffffffffu, s0 >= 0 && s0 < p.num_slots);
+      const unsigned hi = __ballot_sync(0xffffffffu, s1 >= 0 && s1 < p.num_slots);
+      valid = (unsigned long long)lo | ((unsigned long long)hi << 32);
     };
-    auto tile_slots = [&](const Segment& sg, int t, int& s0, int& s1, bool& contiguous, int& first) {
+    auto tile_slots = [&](const Segment& sg, int t, int& s0, int& s1, bool& contiguous, int& first,
+                          unsigned long long& valid) {
       const int key0 = t * kTileKeys;
       const int nvalid = min(kTileKeys, sg.len - key0);
       const int* ip = p.kv_indices + sg.kv0 + key0;
       s0 = lane < nvalid ? __ldg(ip + lane) : p.num_slots;
       s1 = lane + 32 < nvalid ? __ldg(ip + lane + 32) : p.num_slots;
-      eval_slots(nvalid, s0, s1, contiguous, first);
+      eval_slots(nvalid, s0, s1, contiguous, first, valid);
     };
     const bool decode = p.qo_indptr == nullptr;
     const uint64_t kv_policy = l2_policy_evict_first();
@@ -323,14 +334,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       const int stage = j % kStages;
       int s0, s1, first;
       bool contiguous;
+      unsigned long long valid;
       if (kGather && have_next) {
         s0 = next_s0;
         s1 = next_s1;
-        eval_slots(min(kTileKeys, it.seg.len - it.t * kTileKeys), s0, s1, contiguous, first);
+        eval_slots(min(kTileKeys, it.seg.len - it.t * kTileKeys), s0, s1, contiguous, first, valid);
         have_next = false;
       } else {
         // Slot ids first, so their load overlaps the wait for a free stage.
-        tile_slots(it.seg, it.t, s0, s1, contiguous, first);
+        tile_slots(it.seg, it.t, s0, s1, contiguous, first, valid);
       }
       if (j >= kStages &&
           !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout, wait_ns))
@@ -348,6 +360,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         d.flags = (it.first() ? kFirst : 0) | (it.last() ? kLast : 0) | (it.seg.whole ? kWhole : 0) |
                   (contiguous ? 0 : kCopied);
         d.next_row = -1;
+        d.pad = 0;
+        d.valid = valid;
         if (it.last()) {
           TileIter peek = it;
           peek.advance();
@@ -518,7 +532,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       mbar_wait(bar(DRAIN), 0, &no_abort, p.status, kStatusTimeout, wait_ns);
     }
     __syncwarp();
-  } else {
+  } else if (warp < kSoftmaxWarps) {
     // ------------------------------------------------------------ softmax warps
     const int row = threadIdx.x & 127;  // TMEM lane == query head
     const int half = warp >> 2;         // key columns 32*half .. +31 of each tile
@@ -717,12 +731,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         q_pending = -1;
       }
       const int nvalid = min(kTileKeys, (kPack ? cd.len - lag : cd.len) - cd.t * kTileKeys) - 32 * half;
+      const uint32_t vm = static_cast<uint32_t>(cd.valid >> (32 * half));  // keys that are keys of the row
       // All 32 keys valid and a non-negative scale (the usual case): the maximum of the
       // scaled scores is the scaled maximum, and the scale folds into the exponent below.
-      const bool full = nvalid >= 32 && scale >= 0.f;
+      const bool full = nvalid >= 32 && vm == 0xffffffffu && scale >= 0.f;
       if (!full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = k < nvalid ? s[k] * scale : -INFINITY;
+        for (int k = 0; k < 32; ++k) s[k] = (k < nvalid && ((vm >> k) & 1u)) ? s[k] * scale : -INFINITY;
       }
       float mx;
       {  // maximum as a tree (short dependency chains)
@@ -751,8 +766,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
       }
       uint32_t pk[16];
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      // A packed token can see no key of a split segment (m_ref = -inf): its P is zero.
-      const float mref = (kPack && m_ref == -INFINITY) ? 0.f : m_ref;
+      // No key seen yet in this segment (m_ref = -inf: a packed token whose horizon ends
+      // before the segment, or a tile of padding entries): every P is zero.
+      const float mref = m_ref == -INFINITY ? 0.f : m_ref;
       if (full) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -802,7 +818,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGather ? kThreadsGa
         const float lt = l + lbuf[(half ^ 1) * 128 + row];
         if (!mbar_wait(bar(O_FULL), cd.nseg & 1, abort, p.status, kStatusTimeout, wait_ns)) break;
         tc_fence_after();
-        const float inv_l = (kPack && !(lt > 0.f)) ? 0.f : 1.f / lt;  // (no key: out 0, lse -inf)
+        const float inv_l = lt > 0.f ? 1.f / lt : 0.f;  // (no key: out 0, lse -inf)
         const float lse2 = m_ref + fast_log2(lt);
         const bool valid = row < p.heads;
         const size_t frag = ((size_t)w * 2 + cd.slot) * p.heads + row;
@@ -896,7 +912,7 @@ cudaError_t launch_instance(const TmaMaps& maps, const MlaParams& p, cudaStream_
       configured[dev] = true;
     }
   }
-  mla_tc_kernel<kGather, kPack><<<2 * p.workers, kGather ? kThreadsGather : kThreads, kSmemBytes, stream>>>(maps, p);
+  mla_tc_kernel<kGather, kPack><<<2 * p.workers, instance_threads<kGather, kPack>(), kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
 }  // namespace

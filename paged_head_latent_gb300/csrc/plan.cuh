@@ -45,15 +45,23 @@ struct Req {
 };
 
 struct PlanArgs {
-  const int32_t* kv_indptr;
+  const int32_t* kv_indptr;  // nullptr: every row owns `topk` consecutive entries
   const int32_t* qo_indptr;  // nullptr for decode
   int batch;
   int num_kv_indices;
+  int topk;                  // entries per row when kv_indptr is nullptr (sparse decode)
 };
 
 __device__ __forceinline__ Req load_req(const PlanArgs& p, int b) {
   Req r;
-  int k0 = __ldg(p.kv_indptr + b), k1 = __ldg(p.kv_indptr + b + 1);
+  int k0, k1;
+  if (p.kv_indptr) {
+    k0 = __ldg(p.kv_indptr + b);
+    k1 = __ldg(p.kv_indptr + b + 1);
+  } else {  // sparse decode: row b lists its keys in entries b*topk .. b*topk + topk - 1
+    k0 = b * p.topk;
+    k1 = k0 + p.topk;
+  }
   // Clamp so that corrupt indptr never leads to reads outside kv_indices.
   k0 = min(max(k0, 0), p.num_kv_indices);
   k1 = min(max(k1, k0), p.num_kv_indices);

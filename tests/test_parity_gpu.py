@@ -192,6 +192,74 @@ def test_bound_call_repeats_the_call(lib):
         assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
 
 
+# ------------------------------------------------------ sparse (top-k) decode
+
+@pytest.mark.parametrize("kv_lens,topk,heads,s_q,ps", [
+    ([5, 130, 700], 64, 128, 1, 64),    # short requests padded with -1
+    ([300, 1000], 200, 16, 2, 16),      # two query tokens per request, ragged last tile
+    ([2049, 90], 128, 128, 1, 1),       # page size 1
+    ([64], 64, 1, 1, 64),               # one head, exactly one tile
+])
+def test_sparse_small(lib, kv_lens, topk, heads, s_q, ps):
+    w = wl.make_sparse_decode(kv_lens, topk, num_qo_heads=heads, page_size=ps, seed=4200 + topk + heads, s_q=s_q)
+    check_full(lib, w)
+
+
+def test_sparse_out_of_range_and_duplicate_entries(lib):
+    """-1, large and negative entries anywhere in a row are skipped; a duplicate counts twice."""
+    w = wl.make_sparse_decode([400, 250], 96, num_qo_heads=64, page_size=64, seed=4210)
+    idx = w.indices.clone()
+    n = w.num_pages * w.page_size
+    idx[0, 3] = -1
+    idx[0, 40] = n
+    idx[1, 0] = -77
+    idx[1, 90] = n + 1000
+    idx[1, 91] = idx[1, 5]
+    w = dataclasses.replace(w, indices=idx, kv_indices=idx.reshape(-1).clone())
+    check_full(lib, w)
+
+
+@pytest.mark.parametrize("workers", [1, 3, 40])
+def test_sparse_split_count(lib, workers):
+    w = wl.make_sparse_decode([3000, 100, 1500, 20], 700, num_qo_heads=128, page_size=64, seed=4220)
+    check_full(lib, w, num_workers=workers)
+
+
+def test_sparse_row_of_padding_only(lib):
+    w = wl.make_sparse_decode([300, 300, 300], 128, num_qo_heads=32, page_size=64, seed=4230)
+    idx = w.indices.clone()
+    idx[1, :] = -1
+    w = dataclasses.replace(w, indices=idx, kv_indices=idx.reshape(-1).clone())
+    for workers in (0, 5):
+        out, lse = check_full(lib, w, num_workers=workers)
+        assert np.all(out[1] == 0) and np.all(np.isneginf(lse[1]))
+
+
+def test_sparse_nan_in_unreferenced_slots(lib):
+    w = wl.make_sparse_decode([500, 129], 100, num_qo_heads=128, page_size=64, seed=4240)
+    ref_out, ref_lse = oracle_run(w)
+    out, lse = run_gpu(lib, wl.poison_unreferenced(w))
+    assert np.all(np.isfinite(out))
+    assert_close(out, lse, ref_out, ref_lse, "sparse poisoned")
+
+
+def test_decode_skips_out_of_range_slot(lib):
+    """A CSR index outside the cache is not a key of the row (the same rule as sparse
+    padding): the result is the oracle's over the remaining keys."""
+    w = wl.make_decode([70, 200], num_qo_heads=16, page_size=64, seed=4250)
+    bad = w.kv_indices.clone()
+    bad[10] = w.num_pages * w.page_size + 3
+    w_bad = dataclasses.replace(w, kv_indices=bad)
+    keep = torch.ones(bad.numel(), dtype=torch.bool)
+    keep[10] = False
+    ip = w.kv_indptr.clone()
+    ip[1:] -= 1
+    w_ref = dataclasses.replace(w, kv_indices=bad[keep].clone(), kv_indptr=ip)
+    ref_out, ref_lse = oracle_run(w_ref)
+    out, lse = run_gpu(lib, w_bad)
+    assert_close(out, lse, ref_out, ref_lse, "out-of-range slot")
+
+
 # -------------------------------------------------------------- small prefill
 
 @pytest.mark.parametrize("q_lens,prefixes,heads,ps", [
@@ -261,7 +329,7 @@ def test_cuda_graph_capture(lib):
 # and last row of every request, and every row where a split-KV worker's range starts or
 # ends.
 
-FULL_DECODE = ["decode_b64_h128_ps64", "decode_b128_h128_ps1", "decode_b32_h128_skew"]
+FULL_DECODE = ["decode_b64_h128_ps64", "decode_b128_h128_ps1", "decode_b32_h128_skew", "sparse_b64_h128_topk2048"]
 
 
 @pytest.mark.parametrize("name", FULL_DECODE)
