@@ -159,6 +159,46 @@ int mla_paged_decode_sparse(const void* q_nope, const void* q_pe, const void* ck
                             size_t workspace_bytes, int flags, void* stream);
 
 /*
+ * Block-table adapter.  The prims_ts wrapper ("batch_mla_decode_with_paged_kv_cache":
+ * block_tables [batch, max_num_blocks], seq_lens) and FlashMLA's flash_mla_with_kvcache
+ * (block_table, cache_seqlens) name a request's keys as the first seq_len slots of its
+ * pages, in block-table order.  This writes the token-slot CSR the decode calls take:
+ *   len_b = clamp(seq_lens[b], 0, max_blocks * page_size)
+ *   kv_indptr[b] = len_0 + ... + len_{b-1}  (kv_indptr[batch] = the total)
+ *   kv_indices[kv_indptr[b] + k] = block_table[b * max_blocks + k / page_size] * page_size
+ *                                  + k % page_size
+ *   block_table [batch, max_blocks] int32 page ids (row-major; entries past a request's
+ *               last needed block are not read), seq_lens [batch] int32
+ *   kv_indptr [batch + 1] int32 (written), kv_indices [capacity] int32 (written)
+ * A slot that is negative or does not fit in int32 is written as -1, and any slot
+ * outside the cache is skipped by the decode (not a key).  Positions at or past
+ * `capacity` are not written (kv_indptr still counts them; pass capacity as
+ * num_kv_indices and the decode reads no further).  batch * max_blocks * page_size is
+ * always enough.  Two kernel launches on `stream`, no synchronisation; graph-capturable.
+ * Returns MLA_ERR_DIMS (negative sizes, page_size < 1, max_blocks * page_size or
+ * capacity above INT32_MAX), MLA_ERR_NULL, MLA_ERR_LAUNCH, or MLA_OK.
+ */
+int mla_block_table_to_csr(const int32_t* block_table, const int32_t* seq_lens, int batch, int max_blocks,
+                           int page_size, int32_t* kv_indptr, int32_t* kv_indices, long long capacity,
+                           void* stream);
+
+/*
+ * Paged MLA decode from a block table: mla_block_table_to_csr into the workspace, then
+ * mla_paged_decode on that CSR, on `stream`.  Arguments as for mla_paged_decode, with
+ * block_table [batch, max_blocks] and seq_lens [batch] in place of kv_indptr and
+ * kv_indices; dims->num_kv_indices is ignored (the CSR's capacity,
+ * batch * max_blocks * page_size, is used and must fit int32, else MLA_ERR_DIMS).
+ * workspace >= mla_workspace_bytes_block_table(dims, max_blocks) bytes, zero-filled
+ * before first use like the decode's; flags must be 0 (MLA_ERR_DIMS otherwise: the
+ * CSR ends short of its capacity, which MLA_VALIDATE would report).
+ */
+size_t mla_workspace_bytes_block_table(const mla_dims* dims, int max_blocks);
+int mla_paged_decode_block_table(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                                 const void* kpe_cache, const int32_t* block_table, const int32_t* seq_lens,
+                                 int max_blocks, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                                 void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
  * Paged MLA decode for callers that cannot allocate device memory (a plugin that runs
  * inside another framework's memory pool, code that must not call cudaMalloc after
  * start-up, or a context where an allocation would synchronise the device).  This entry

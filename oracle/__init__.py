@@ -4,9 +4,10 @@ Only tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of ``bench.py``
 may import this package.  It shares no code with the CUDA path.
 """
 
-from .mla_oracle import (attend, combine_partials, mla_decode, mla_decode_split, mla_prefill,
-                         mla_sparse_decode, online_softmax_partial, scores, visible_len)
+from .mla_oracle import (attend, block_table_to_csr, combine_partials, mla_decode, mla_decode_block_table,
+                         mla_decode_split, mla_prefill, mla_sparse_decode, online_softmax_partial, scores,
+                         visible_len)
 from .brute import brute_decode, brute_prefill
 
-__all__ = ["attend", "combine_partials", "mla_decode", "mla_decode_split", "mla_prefill", "mla_sparse_decode",
+__all__ = ["attend", "block_table_to_csr", "mla_decode_block_table", "combine_partials", "mla_decode", "mla_decode_split", "mla_prefill", "mla_sparse_decode",
            "online_softmax_partial", "scores", "visible_len", "brute_decode", "brute_prefill"]

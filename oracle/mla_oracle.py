@@ -111,6 +111,47 @@ def mla_decode(q_nope, q_pe, ckv_cache, kpe_cache, kv_indptr, kv_indices, sm_sca
     return out, lse
 
 
+def block_table_to_csr(block_table, seq_lens, page_size):
+    """Token-slot CSR of a block table.
+
+    The prims_ts wrapper ("batch_mla_decode_with_paged_kv_cache": block_tables
+    [batch, max_num_blocks], seq_lens) and FlashMLA's ``flash_mla_with_kvcache``
+    (block_table, cache_seqlens) name a request's keys as the first seq_len slots of its
+    pages, taken in table order; a slot is page * page_size + offset (FlashMLA notes, "FP8
+    KV Cache Quantization and Dequantization", physical index).  A length is clamped to
+    [0, max_blocks * page_size]; a slot that is negative or above the int32 range is
+    written as -1 (not a key).  Returns (kv_indptr [batch + 1], kv_indices), int64 numpy.
+    """
+    table = np.asarray(block_table, dtype=np.int64)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    indptr = [0]
+    indices = []
+    for b in range(table.shape[0]):
+        n = min(max(int(lens[b]), 0), table.shape[1] * page_size)
+        for k in range(n):
+            slot = int(table[b, k // page_size]) * page_size + k % page_size
+            indices.append(slot if 0 <= slot <= 2 ** 31 - 1 else -1)
+        indptr.append(len(indices))
+    return np.asarray(indptr, dtype=np.int64), np.asarray(indices, dtype=np.int64)
+
+
+def mla_decode_block_table(q_nope, q_pe, ckv_cache, kpe_cache, block_table, seq_lens, sm_scale):
+    """Decode whose keys come from a block table (``block_table_to_csr``).  A slot outside
+    the cache is not a key of the row (the reading the sparse page's -1 padding implies),
+    so such entries are dropped before ``mla_decode``."""
+    page_size = np.asarray(ckv_cache).shape[1]
+    num_slots = np.asarray(ckv_cache).shape[0] * page_size
+    indptr, indices = block_table_to_csr(block_table, seq_lens, page_size)
+    kept_ptr = [0]
+    kept = []
+    for b in range(len(indptr) - 1):
+        row = [int(t) for t in indices[indptr[b]:indptr[b + 1]] if 0 <= t < num_slots]
+        kept.extend(row)
+        kept_ptr.append(len(kept))
+    return mla_decode(q_nope, q_pe, ckv_cache, kpe_cache, np.asarray(kept_ptr), np.asarray(kept, dtype=np.int64),
+                      sm_scale)
+
+
 def visible_len(kv_len, q_len, i):
     """Keys visible to query i of a request (causal, bottom-right aligned)."""
     return kv_len - q_len + i + 1

@@ -55,6 +55,12 @@ _SIGNATURES = [
     ("mla_paged_decode_sparse", ctypes.c_int,
      [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
       ctypes.c_int, _P]),
+    ("mla_block_table_to_csr", ctypes.c_int,
+     [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_longlong, _P]),
+    ("mla_workspace_bytes_block_table", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
+    ("mla_paged_decode_block_table", ctypes.c_int,
+     [_P, _P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
+      ctypes.c_int, _P]),
     ("mla_paged_decode_noalloc", ctypes.c_int,
      [_P, _P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), ctypes.c_int, _P]),
     ("mla_workspace_bytes", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
@@ -306,6 +312,77 @@ def mla_paged_decode_sparse(q_nope, q_pe, ckv_cache, kpe_cache, indices, sm_scal
                                            ctypes.c_void_p(stream.cuda_stream))
     if st != 0:
         raise MlaError(st, "mla_paged_decode_sparse")
+    return out, lse
+
+
+def block_table_to_csr(block_table, seq_lens, page_size, capacity=None, stream=None):
+    """Token-slot CSR (kv_indptr [batch + 1], kv_indices [capacity]) of a block table
+    [batch, max_blocks] and seq_lens [batch] (int32, on the GPU): request b's keys are the
+    first seq_lens[b] slots of its pages in table order.  capacity defaults to
+    batch * max_blocks * page_size; entries past the total are left unset."""
+    _check_cuda("block_table", block_table, torch.int32)
+    _check_cuda("seq_lens", seq_lens, torch.int32)
+    if block_table.dim() != 2 or seq_lens.shape != (block_table.shape[0],):
+        raise ValueError("block_table must be [batch, max_blocks] and seq_lens [batch]")
+    batch, max_blocks = block_table.shape
+    if capacity is None:
+        capacity = batch * max_blocks * page_size
+    dev = block_table.device
+    kv_indptr = torch.empty(batch + 1, dtype=torch.int32, device=dev)
+    kv_indices = torch.empty(max(int(capacity), 1), dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = lib().mla_block_table_to_csr(_ptr(block_table), _ptr(seq_lens), int(batch), int(max_blocks),
+                                          int(page_size), _ptr(kv_indptr), _ptr(kv_indices), int(capacity),
+                                          ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise MlaError(st, "mla_block_table_to_csr")
+    return kv_indptr, kv_indices[:int(capacity)]
+
+
+def mla_paged_decode_block_table(q_nope, q_pe, ckv_cache, kpe_cache, block_table, seq_lens, sm_scale, out=None,
+                                 lse=None, workspace=None, num_workers=0,
+                                 stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA decode from a block table [batch, max_blocks] and seq_lens [batch]
+    (int32): the conversion to the token-slot CSR and the decode in one call.
+    Returns (out [batch, H, 512], lse [batch, H])."""
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe), ("ckv_cache", ckv_cache), ("kpe_cache", kpe_cache)):
+        _check_cuda(n, t, torch.bfloat16)
+    _check_cuda("block_table", block_table, torch.int32)
+    _check_cuda("seq_lens", seq_lens, torch.int32)
+    batch, heads = q_nope.shape[0], q_nope.shape[1]
+    if q_nope.shape != (batch, heads, HEAD_DIM_CKV) or q_pe.shape != (batch, heads, HEAD_DIM_KPE):
+        raise ValueError("q_nope must be [batch, H, 512] and q_pe [batch, H, 64]")
+    if block_table.dim() != 2 or block_table.shape[0] != batch or seq_lens.shape != (batch,):
+        raise ValueError("block_table must be [batch, max_blocks] and seq_lens [batch]")
+    max_blocks = block_table.shape[1]
+    num_pages, page_size = _cache_geometry(ckv_cache, kpe_cache)
+    dims = make_dims(batch, heads, num_pages, page_size, 0, num_workers=num_workers)
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty(batch, heads, HEAD_DIM_CKV, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(batch, heads, dtype=torch.float32, device=dev)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("lse", lse, torch.float32)
+    if out.shape != (batch, heads, HEAD_DIM_CKV) or lse.shape != (batch, heads):
+        raise ValueError("out must be [batch, H, 512] and lse [batch, H]")
+    need = lib().mla_workspace_bytes_block_table(ctypes.byref(dims), int(max_blocks))
+    if need == 0:
+        raise MlaError(-2, "mla_workspace_bytes_block_table")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        st = lib().mla_paged_decode_block_table(_ptr(q_nope), _ptr(q_pe), _ptr(ckv_cache), _ptr(kpe_cache),
+                                                _ptr(block_table), _ptr(seq_lens), int(max_blocks),
+                                                float(sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims),
+                                                _ptr(workspace), workspace.numel(), 0,
+                                                ctypes.c_void_p(stream.cuda_stream))
+    if st != 0:
+        raise MlaError(st, "mla_paged_decode_block_table")
     return out, lse
 
 

@@ -324,6 +324,79 @@ int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cach
              out, lse, dims, workspace, workspace_bytes, flags, stream);
 }
 
+int mla_block_table_to_csr(const int32_t* block_table, const int32_t* seq_lens, int batch, int max_blocks,
+                           int page_size, int32_t* kv_indptr, int32_t* kv_indices, long long capacity,
+                           void* stream) {
+  if (batch < 0 || max_blocks < 0 || page_size < 1 || capacity < 0) return MLA_ERR_DIMS;
+  if ((long long)max_blocks * page_size > 0x7fffffffLL || capacity > 0x7fffffffLL) return MLA_ERR_DIMS;
+  if (!kv_indptr) return MLA_ERR_NULL;
+  if (batch > 0 && (!seq_lens || (max_blocks > 0 && !block_table))) return MLA_ERR_NULL;
+  if (capacity > 0 && !kv_indices) return MLA_ERR_NULL;
+  if (mla::launch_block_table_csr(block_table, seq_lens, batch, max_blocks, page_size, kv_indptr, kv_indices,
+                                  capacity, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_LAUNCH;
+  return MLA_OK;
+}
+
+}  // extern "C"
+
+namespace {
+// Workspace of the block-table decode: the decode's own workspace, then the CSR the
+// adapter writes (kv_indptr, then kv_indices with room for every block of every row).
+struct BlockTableLayout {
+  size_t decode, indptr, indices, total;
+  long long capacity;
+  BlockTableLayout(size_t decode_bytes, int batch, int max_blocks, int page_size) {
+    capacity = (long long)batch * max_blocks * page_size;
+    decode = mla::align_up(decode_bytes, 256);
+    indptr = decode;
+    indices = mla::align_up(indptr + ((size_t)batch + 1) * sizeof(int32_t), 256);
+    total = mla::align_up(indices + (size_t)capacity * sizeof(int32_t), 256);
+  }
+};
+
+// The decode dims with the capacity as num_kv_indices; false if it does not fit int32.
+bool block_table_dims(const mla_dims* dims, int max_blocks, mla_dims* d) {
+  if (!dims || max_blocks < 0) return false;
+  const long long cap = (long long)dims->batch * max_blocks * dims->page_size;
+  if (dims->batch < 0 || dims->page_size < 1 || cap > 0x7fffffffLL) return false;
+  *d = *dims;
+  d->num_kv_indices = (int)cap;
+  return true;
+}
+}  // namespace
+
+extern "C" {
+
+size_t mla_workspace_bytes_block_table(const mla_dims* dims, int max_blocks) {
+  mla_dims d;
+  if (!block_table_dims(dims, max_blocks, &d)) return 0;
+  const size_t base = mla_workspace_bytes(&d, 0);
+  if (base == 0) return 0;
+  return BlockTableLayout(base, d.batch, max_blocks, d.page_size).total;
+}
+
+int mla_paged_decode_block_table(const void* q_nope, const void* q_pe, const void* ckv_cache,
+                                 const void* kpe_cache, const int32_t* block_table, const int32_t* seq_lens,
+                                 int max_blocks, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                                 void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  if (!dims) return MLA_ERR_NULL;
+  mla_dims d;
+  if (flags != 0 || !block_table_dims(dims, max_blocks, &d)) return MLA_ERR_DIMS;
+  const size_t base = mla_workspace_bytes(&d, 0);
+  if (base == 0) return check_dims(&d, false) != MLA_OK ? check_dims(&d, false) : MLA_ERR_DIMS;
+  const BlockTableLayout lay(base, d.batch, max_blocks, d.page_size);
+  if (!workspace || workspace_bytes < lay.total) return MLA_ERR_WORKSPACE;
+  auto* ws = static_cast<uint8_t*>(workspace);
+  int32_t* indptr = reinterpret_cast<int32_t*>(ws + lay.indptr);
+  int32_t* indices = reinterpret_cast<int32_t*>(ws + lay.indices);
+  const int st = mla_block_table_to_csr(block_table, seq_lens, d.batch, max_blocks, d.page_size, indptr, indices,
+                                        lay.capacity, stream);
+  if (st != MLA_OK) return st;
+  return run(false, 0, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, indptr, indices, sm_scale, out, lse, &d,
+             workspace, lay.decode, 0, stream);
+}
+
 size_t mla_workspace_bytes(const mla_dims* dims, int is_prefill) {
   if (check_dims(dims, is_prefill != 0) != MLA_OK) return 0;
   int G = 0;

@@ -189,6 +189,60 @@ def make_decode(kv_lens: Sequence[int], num_qo_heads: int, page_size: int, seed:
                     ckv_cache=ckv, kpe_cache=kpe, kv_indptr=indptr, kv_indices=indices)
 
 
+@dataclasses.dataclass
+class BlockTableInputs:
+    """Decode inputs in block-table form (the prims_ts wrapper's block_tables
+    [batch, max_num_blocks] and seq_lens; FlashMLA's block_table and cache_seqlens)."""
+
+    num_qo_heads: int
+    page_size: int
+    num_pages: int
+    sm_scale: float
+    q_nope: torch.Tensor
+    q_pe: torch.Tensor
+    ckv_cache: torch.Tensor
+    kpe_cache: torch.Tensor
+    block_table: torch.Tensor  # [batch, max_blocks] int32 page ids
+    seq_lens: torch.Tensor     # [batch] int32
+
+    def to(self, device) -> "BlockTableInputs":
+        return dataclasses.replace(self, **{f.name: getattr(self, f.name).to(device)
+                                            for f in dataclasses.fields(self)
+                                            if isinstance(getattr(self, f.name), torch.Tensor)})
+
+
+def make_block_table_decode(seq_lens: Sequence[int], num_qo_heads: int, page_size: int, max_blocks: int,
+                            seed: int, junk: str = "random", sm_scale: float = DEFAULT_SM_SCALE) -> BlockTableInputs:
+    """Block-table decode inputs: request b's ceil(len_b / page_size) pages (len_b its
+    sequence length, clamped to the table's width) are drawn from a permuted pool and
+    fill the front of row b; the rest of the row holds ``junk``: random page ids of the
+    pool ("random") or -1 ("minus1"), which a correct reader never uses.  A sequence
+    length may be negative or exceed max_blocks * page_size (the reader clamps it).
+    Draw order: page permutation, junk, q_nope, q_pe, ckv_cache, kpe_cache."""
+    gen = torch.Generator().manual_seed(seed)
+    lens = [min(max(int(x), 0), max_blocks * page_size) for x in seq_lens]
+    need = [-(-l // page_size) for l in lens]
+    num_pages = max(sum(need), 1)
+    perm = torch.randperm(num_pages, generator=gen, dtype=torch.int64)
+    b = len(lens)
+    if junk == "random":
+        table = torch.randint(0, num_pages, (b, max_blocks), generator=gen, dtype=torch.int64)
+    else:
+        table = torch.full((b, max_blocks), -1, dtype=torch.int64)
+    p0 = 0
+    for r, n in enumerate(need):
+        table[r, :n] = perm[p0:p0 + n]
+        p0 += n
+    q_nope = _randn_bf16((b, num_qo_heads, HEAD_DIM_CKV), gen)
+    q_pe = _randn_bf16((b, num_qo_heads, HEAD_DIM_KPE), gen)
+    ckv = _randn_bf16((num_pages, page_size, HEAD_DIM_CKV), gen)
+    kpe = _randn_bf16((num_pages, page_size, HEAD_DIM_KPE), gen)
+    return BlockTableInputs(num_qo_heads=num_qo_heads, page_size=page_size, num_pages=num_pages,
+                            sm_scale=sm_scale, q_nope=q_nope, q_pe=q_pe, ckv_cache=ckv, kpe_cache=kpe,
+                            block_table=table.to(torch.int32).contiguous(),
+                            seq_lens=torch.tensor([int(x) for x in seq_lens], dtype=torch.int32))
+
+
 def make_prefill(q_lens: Sequence[int], prefixes: Sequence[int], num_qo_heads: int,
                  page_size: int, seed: int, pool_pages: Optional[int] = None,
                  token_shuffle: bool = False, sm_scale: float = DEFAULT_SM_SCALE,
