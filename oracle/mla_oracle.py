@@ -152,6 +152,62 @@ def mla_decode_block_table(q_nope, q_pe, ckv_cache, kpe_cache, block_table, seq_
                       sm_scale)
 
 
+FP8_TOKEN_BYTES = 656  # 512 e4m3 + 4 fp32 scales + 64 bf16 (FlashMLA notes, V32_FP8Sparse)
+
+
+def e4m3_to_float(codes):
+    """Value of FP8 E4M3 codes (uint8), from the format's definition: 1 sign bit, 4
+    exponent bits with bias 7, 3 mantissa bits; exponent 0 is subnormal
+    (mantissa / 8 * 2^-6); no infinities; S.1111.111 is NaN.  Returns float64."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 0x7
+    normal = (1.0 + m / 8.0) * np.exp2(e - 7.0)
+    sub = (m / 8.0) * 2.0 ** -6
+    v = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 0xF) & (m == 0x7), np.nan, v)
+
+
+def _round_bf16(x32):
+    """float32 -> nearest bfloat16 (ties to even), returned as float64."""
+    import torch  # a library primitive for the rounding step only
+    return torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32)).to(torch.bfloat16).double().numpy()
+
+
+def dequantize_fp8_cache(kv_fp8):
+    """The 656-byte-per-token cache (FlashMLA notes, "FP8 KV Cache Quantization and
+    Dequantization", V32_FP8Sparse: bytes 0-511 the 512-wide latent as E4M3, bytes
+    512-527 four float32 scales, one per 128-element tile, bytes 528-655 the 64-wide
+    rope part in bfloat16, unquantised) back to BF16, as the page's dequantize
+    returns: latent element i of a token = bf16(float32(e4m3_i) * scale_{i // 128}),
+    the product in float32.  kv_fp8 [P, ps, 656] uint8.  Returns (ckv [P, ps, 512],
+    kpe [P, ps, 64]) float64 holding bf16 values."""
+    raw = np.asarray(kv_fp8, dtype=np.uint8)
+    assert raw.shape[-1] == FP8_TOKEN_BYTES
+    lead = raw.shape[:-1]
+    vals = e4m3_to_float(raw[..., :512]).astype(np.float32)  # exact: E4M3 fits in float32
+    scales = np.ascontiguousarray(raw[..., 512:528]).view(np.float32).reshape(*lead, 4)
+    prod = (vals.reshape(*lead, 4, 128) * scales[..., None]).astype(np.float32).reshape(*lead, 512)
+    ckv = _round_bf16(prod)
+    rope = np.ascontiguousarray(raw[..., 528:656]).view(np.uint16).reshape(*lead, 64).astype(np.uint32) << 16
+    kpe = rope.view(np.float32).astype(np.float64)
+    return ckv, kpe
+
+
+def mla_decode_fp8(q_nope, q_pe, kv_fp8, kv_indptr, kv_indices, sm_scale):
+    """Decode over an FP8 cache: the dense decode of the dequantised cache."""
+    ckv, kpe = dequantize_fp8_cache(kv_fp8)
+    return mla_decode(q_nope, q_pe, ckv, kpe, kv_indptr, kv_indices, sm_scale)
+
+
+def mla_sparse_decode_fp8(q_nope, q_pe, kv_fp8, indices, sm_scale):
+    """Sparse decode over an FP8 cache (FlashMLA notes, "flash_mla_with_kvcache (Sparse
+    Attention with FP8 KV Cache)"): the sparse decode of the dequantised cache."""
+    ckv, kpe = dequantize_fp8_cache(kv_fp8)
+    return mla_sparse_decode(q_nope, q_pe, ckv, kpe, indices, sm_scale)
+
+
 def visible_len(kv_len, q_len, i):
     """Keys visible to query i of a request (causal, bottom-right aligned)."""
     return kv_len - q_len + i + 1

@@ -57,6 +57,11 @@ class Workload:
     # cache are padding.  kv_indptr / kv_indices then hold the same lists as a CSR view
     # (row r owns entries r*topk .. r*topk + topk - 1).
     indices: Optional[torch.Tensor] = None
+    # FP8 cache (kinds "decode_fp8" / "sparse_fp8"): [num_pages, page_size, 656] uint8 per
+    # token -- 512 E4M3 latent values, 4 float32 scales (one per 128 values), 64 bf16
+    # rope values (FlashMLA's V32_FP8Sparse layout).  ckv_cache / kpe_cache then hold the
+    # bf16 values it was quantised from.
+    kv_fp8: Optional[torch.Tensor] = None
 
     @property
     def batch(self) -> int:
@@ -97,9 +102,9 @@ class Workload:
 
     def visible_keys(self) -> int:
         """Number of (query row, key) pairs the operator scores, per head."""
-        if self.kind == "decode":
+        if self.kind in ("decode", "decode_fp8"):
             return sum(self.kv_lens())
-        if self.kind == "sparse":
+        if self.kind in ("sparse", "sparse_fp8"):
             return sum(self.valid_per_row())
         total = 0
         for ql, kl in zip(self.q_lens(), self.kv_lens()):
@@ -115,6 +120,8 @@ class Workload:
             d["qo_indptr"] = self.qo_indptr
         if self.indices is not None:
             d["indices"] = self.indices
+        if self.kv_fp8 is not None:
+            d["kv_fp8"] = self.kv_fp8
         return d
 
     def to(self, device) -> "Workload":
@@ -384,6 +391,33 @@ def sparse_b64_h128_topk2048() -> Workload:
                               name="sparse_b64_h128_topk2048")
 
 
+FP8_TOKEN_BYTES = 656
+
+
+def quantize_fp8(w: Workload, name: Optional[str] = None) -> Workload:
+    """The workload with its cache in the 656-byte FP8 layout.  Each token's 512 latent
+    values are quantised in tiles of 128: scale = max|x| / 448 (1 for an all-zero tile),
+    code = E4M3 nearest to x / scale (clamped to +-448); the rope part stays bf16.  This
+    only prepares inputs; how the cache is read back is the reader's business."""
+    ckv = w.ckv_cache.float()
+    lead = ckv.shape[:-1]
+    tiles = ckv.reshape(*lead, 4, 128)
+    amax = tiles.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / 448.0, torch.ones_like(amax)).to(torch.float32)
+    codes = (tiles / scale[..., None]).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    buf = torch.empty(*lead, FP8_TOKEN_BYTES, dtype=torch.uint8)
+    buf[..., :512] = codes.reshape(*lead, 512).view(torch.uint8)
+    buf[..., 512:528] = scale.contiguous().view(torch.uint8).reshape(*lead, 16)
+    buf[..., 528:] = w.kpe_cache.contiguous().view(torch.uint8).reshape(*lead, 128)
+    kind = {"decode": "decode_fp8", "sparse": "sparse_fp8"}[w.kind]
+    return dataclasses.replace(w, kind=kind, kv_fp8=buf, name=name or (w.name + "_fp8"))
+
+
+def fp8_b64_h128_ps64() -> Workload:
+    """The 64-request, 128-head, page-64 decode batch with its cache in FP8."""
+    return quantize_fp8(decode_b64_h128_ps64(), name="fp8_b64_h128_ps64")
+
+
 NAMED = {
     "decode_b4_h16_ps64": decode_b4_h16_ps64,
     "decode_b64_h128_ps64": decode_b64_h128_ps64,
@@ -392,6 +426,7 @@ NAMED = {
     "prefill_causal_h128": prefill_causal_h128,
     "mtp_b64_h16_q4_ps64": mtp_b64_h16_q4_ps64,
     "sparse_b64_h128_topk2048": sparse_b64_h128_topk2048,
+    "fp8_b64_h128_ps64": fp8_b64_h128_ps64,
 }
 
 
