@@ -159,6 +159,31 @@ int mla_paged_decode_sparse(const void* q_nope, const void* q_pe, const void* ck
                             size_t workspace_bytes, int flags, void* stream);
 
 /*
+ * Paged MLA decode over an FP8 KV cache (FlashMLA notes, "FP8 KV Cache Quantization
+ * and Dequantization", layout V32_FP8Sparse; "flash_mla_with_kvcache" with
+ * is_fp8_kvcache).  kv_fp8 [num_pages * page_size][656] bytes, 16-byte aligned: per
+ * token, bytes 0-511 the 512 latent values as E4M3, bytes 512-527 four float32 scales
+ * (one per 128 latent values), bytes 528-655 the 64 rope values as bf16.  Latent value
+ * i of a token is read as bf16(float32(e4m3_i) * scale[i / 128]) (product in float32,
+ * both roundings to nearest even), the BF16 that the page's dequantisation returns;
+ * the attention is then exactly mla_paged_decode's over those values.  Other arguments
+ * as for mla_paged_decode (same workspace size).  MLA_ERR_ALIGN if kv_fp8 is not
+ * 16-byte aligned.  Codes 0x7F / 0xFF (E4M3 NaN) propagate as NaN.
+ */
+int mla_paged_decode_fp8(const void* q_nope, const void* q_pe, const void* kv_fp8, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                         void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
+ * Sparse (top-k) decode over an FP8 KV cache (FlashMLA notes, "flash_mla_with_kvcache
+ * (Sparse Attention with FP8 KV Cache)"): mla_paged_decode_sparse's arguments with the
+ * cache of mla_paged_decode_fp8.
+ */
+int mla_paged_decode_sparse_fp8(const void* q_nope, const void* q_pe, const void* kv_fp8, const int32_t* indices,
+                                int topk, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                                void* workspace, size_t workspace_bytes, int flags, void* stream);
+
+/*
  * Block-table adapter.  The prims_ts wrapper ("batch_mla_decode_with_paged_kv_cache":
  * block_tables [batch, max_num_blocks], seq_lens) and FlashMLA's flash_mla_with_kvcache
  * (block_table, cache_seqlens) name a request's keys as the first seq_len slots of its

@@ -55,6 +55,11 @@ _SIGNATURES = [
     ("mla_paged_decode_sparse", ctypes.c_int,
      [_P, _P, _P, _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
       ctypes.c_int, _P]),
+    ("mla_paged_decode_fp8", ctypes.c_int,
+     [_P, _P, _P, _P, _P, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t, ctypes.c_int, _P]),
+    ("mla_paged_decode_sparse_fp8", ctypes.c_int,
+     [_P, _P, _P, _P, ctypes.c_int, ctypes.c_float, _P, _P, ctypes.POINTER(MlaDims), _P, ctypes.c_size_t,
+      ctypes.c_int, _P]),
     ("mla_block_table_to_csr", ctypes.c_int,
      [_P, _P, ctypes.c_int, ctypes.c_int, ctypes.c_int, _P, _P, ctypes.c_longlong, _P]),
     ("mla_workspace_bytes_block_table", ctypes.c_size_t, [ctypes.POINTER(MlaDims), ctypes.c_int]),
@@ -315,6 +320,78 @@ def mla_paged_decode_sparse(q_nope, q_pe, ckv_cache, kpe_cache, indices, sm_scal
     return out, lse
 
 
+FP8_TOKEN_BYTES = 656
+
+
+def _fp8_call(name, q_nope, q_pe, kv_fp8, kv_indptr, kv_indices, topk, sm_scale, out, lse, workspace, flags,
+              num_workers, stream):
+    for n, t in (("q_nope", q_nope), ("q_pe", q_pe)):
+        _check_cuda(n, t, torch.bfloat16)
+    _check_cuda("kv_fp8", kv_fp8, torch.uint8)
+    _check_cuda("kv_indices", kv_indices, torch.int32)
+    if kv_fp8.dim() != 3 or kv_fp8.shape[2] != FP8_TOKEN_BYTES:
+        raise ValueError("kv_fp8 must be [num_pages, page_size, 656] uint8")
+    rows, heads = q_nope.shape[0], q_nope.shape[1]
+    if q_nope.shape != (rows, heads, HEAD_DIM_CKV) or q_pe.shape != (rows, heads, HEAD_DIM_KPE):
+        raise ValueError("q_nope must be [rows, H, 512] and q_pe [rows, H, 64]")
+    num_pages, page_size = kv_fp8.shape[0], kv_fp8.shape[1]
+    if topk:
+        if kv_indices.shape != (rows, topk):
+            raise ValueError("indices must be [rows, topk]")
+        n_idx = rows * topk
+    else:
+        _check_cuda("kv_indptr", kv_indptr, torch.int32)
+        if kv_indptr.numel() != rows + 1:
+            raise ValueError("decode: q_nope.shape[0] must equal len(kv_indptr) - 1")
+        n_idx = kv_indices.numel()
+    dims = make_dims(rows, heads, num_pages, page_size, n_idx, num_workers=num_workers)
+    dev = q_nope.device
+    if out is None:
+        out = torch.empty(rows, heads, HEAD_DIM_CKV, dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty(rows, heads, dtype=torch.float32, device=dev)
+    _check_cuda("out", out, torch.bfloat16)
+    _check_cuda("lse", lse, torch.float32)
+    if out.shape != (rows, heads, HEAD_DIM_CKV) or lse.shape != (rows, heads):
+        raise ValueError("out must be [rows, H, 512] and lse [rows, H]")
+    need = workspace_bytes(dims, False)
+    if need == 0:
+        raise MlaError(-2, "mla_workspace_bytes")
+    if workspace is None:
+        workspace = torch.zeros(need, dtype=torch.uint8, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+    with torch.cuda.device(dev):
+        if topk:
+            st = lib().mla_paged_decode_sparse_fp8(_ptr(q_nope), _ptr(q_pe), _ptr(kv_fp8), _ptr(kv_indices),
+                                                   int(topk), float(sm_scale), _ptr(out), _ptr(lse),
+                                                   ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                                                   int(flags), sp)
+        else:
+            st = lib().mla_paged_decode_fp8(_ptr(q_nope), _ptr(q_pe), _ptr(kv_fp8), _ptr(kv_indptr),
+                                            _ptr(kv_indices), float(sm_scale), _ptr(out), _ptr(lse),
+                                            ctypes.byref(dims), _ptr(workspace), workspace.numel(), int(flags), sp)
+    if st != 0:
+        raise MlaError(st, name)
+    return out, lse
+
+
+def mla_paged_decode_fp8(q_nope, q_pe, kv_fp8, kv_indptr, kv_indices, sm_scale, out=None, lse=None,
+                         workspace=None, flags=0, num_workers=0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Paged MLA decode over an FP8 cache kv_fp8 [num_pages, page_size, 656] uint8 (512
+    E4M3 latent values, 4 float32 scales, 64 bf16 rope values per token)."""
+    return _fp8_call("mla_paged_decode_fp8", q_nope, q_pe, kv_fp8, kv_indptr, kv_indices, 0, sm_scale, out, lse,
+                     workspace, flags, num_workers, stream)
+
+
+def mla_paged_decode_sparse_fp8(q_nope, q_pe, kv_fp8, indices, sm_scale, out=None, lse=None, workspace=None,
+                                flags=0, num_workers=0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Sparse (top-k) decode over an FP8 cache: indices [rows, topk] int32 token slots."""
+    return _fp8_call("mla_paged_decode_sparse_fp8", q_nope, q_pe, kv_fp8, None, indices, indices.shape[1],
+                     sm_scale, out, lse, workspace, flags, num_workers, stream)
+
+
 def block_table_to_csr(block_table, seq_lens, page_size, capacity=None, stream=None):
     """Token-slot CSR (kv_indptr [batch + 1], kv_indices [capacity]) of a block table
     [batch, max_blocks] and seq_lens [batch] (int32, on the GPU): request b's keys are the
@@ -455,8 +532,18 @@ def bind_workload(w, out, lse, workspace, stream, flags=0, num_workers=0):
     dims = workload_dims(w, num_workers)
     sp = ctypes.c_void_p(stream.cuda_stream)
     name = {"decode": "mla_paged_decode", "prefill": "mla_paged_prefill", "mtp": "mla_paged_decode_mtp",
-            "sparse": "mla_paged_decode_sparse"}[w.kind]
-    if w.kind == "sparse":
+            "sparse": "mla_paged_decode_sparse", "decode_fp8": "mla_paged_decode_fp8",
+            "sparse_fp8": "mla_paged_decode_sparse_fp8"}[w.kind]
+    if w.kind == "decode_fp8":
+        fn = lib().mla_paged_decode_fp8
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.kv_fp8), _ptr(w.kv_indptr), _ptr(w.kv_indices),
+                float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace), workspace.numel(),
+                int(flags), sp)
+    elif w.kind == "sparse_fp8":
+        fn = lib().mla_paged_decode_sparse_fp8
+        args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.kv_fp8), _ptr(w.indices), int(w.topk), float(w.sm_scale),
+                _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace), workspace.numel(), int(flags), sp)
+    elif w.kind == "sparse":
         fn = lib().mla_paged_decode_sparse
         args = (_ptr(w.q_nope), _ptr(w.q_pe), _ptr(w.ckv_cache), _ptr(w.kpe_cache), _ptr(w.indices),
                 int(w.topk), float(w.sm_scale), _ptr(out), _ptr(lse), ctypes.byref(dims), _ptr(workspace),
@@ -498,6 +585,12 @@ def run_workload(w, out=None, lse=None, workspace=None, flags=0, num_workers=0, 
                                       w.ckv_cache, w.kpe_cache, w.kv_indptr, w.kv_indices, w.sm_scale,
                                       o4, l3, workspace, flags, num_workers, stream)
         return o4.view(b * q, h, HEAD_DIM_CKV), l3.view(b * q, h)
+    if w.kind == "decode_fp8":
+        return mla_paged_decode_fp8(w.q_nope, w.q_pe, w.kv_fp8, w.kv_indptr, w.kv_indices, w.sm_scale,
+                                    out, lse, workspace, flags, num_workers, stream)
+    if w.kind == "sparse_fp8":
+        return mla_paged_decode_sparse_fp8(w.q_nope, w.q_pe, w.kv_fp8, w.indices, w.sm_scale,
+                                           out, lse, workspace, flags, num_workers, stream)
     if w.kind == "sparse":
         return mla_paged_decode_sparse(w.q_nope, w.q_pe, w.ckv_cache, w.kpe_cache, w.indices, w.sm_scale,
                                        out, lse, workspace, flags, num_workers, stream)

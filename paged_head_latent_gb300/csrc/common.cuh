@@ -52,6 +52,9 @@ struct MlaParams {
   unsigned long long wait_ns;
   int fault_skip_tile;
   int topk;  // sparse decode: entries per row (kv_indptr is nullptr); 0 otherwise
+  // FP8 cache, or nullptr: [num_slots][656] bytes per token -- 512 E4M3 latent values,
+  // 4 float32 scales (one per 128 values), 64 bf16 rope values.  ckv / kpe are unused.
+  const uint8_t* kv_fp8;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

@@ -195,7 +195,8 @@ int packed_heads(const mla_dims* d, int q_len) { return q_len > 0 ? q_len * d->n
 int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const void* ckv_cache,
         const void* kpe_cache, const int32_t* qo_indptr, const int32_t* kv_indptr,
         const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
-        void* workspace, size_t workspace_bytes, int flags, void* stream_ptr, int topk = 0) {
+        void* workspace, size_t workspace_bytes, int flags, void* stream_ptr, int topk = 0,
+        const void* kv_fp8 = nullptr) {
   int st = check_dims(dims, prefill);
   if (st != MLA_OK) return st;
   if (topk < 0) return MLA_ERR_DIMS;
@@ -205,11 +206,11 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   const long long rows = prefill ? dims->total_q : dims->batch;
   if (!q_nope || !q_pe || (!kv_indptr && topk == 0) || !out || !lse) return MLA_ERR_NULL;
   // The caches may be NULL only when they hold no slot at all.
-  if ((!ckv_cache || !kpe_cache) && dims->num_pages > 0) return MLA_ERR_NULL;
+  if ((kv_fp8 ? !kv_fp8 : (!ckv_cache || !kpe_cache)) && dims->num_pages > 0) return MLA_ERR_NULL;
   if (prefill && !qo_indptr) return MLA_ERR_NULL;
   if (dims->num_kv_indices > 0 && !kv_indices) return MLA_ERR_NULL;
   if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(ckv_cache) || !aligned16(kpe_cache) ||
-      !aligned16(out))
+      !aligned16(kv_fp8) || !aligned16(out))
     return MLA_ERR_ALIGN;
   if (!std::isfinite(sm_scale)) return MLA_ERR_DIMS;
   int G = 0;
@@ -229,6 +230,7 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   p.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
   p.ckv = static_cast<const __nv_bfloat16*>(ckv_cache);
   p.kpe = static_cast<const __nv_bfloat16*>(kpe_cache);
+  p.kv_fp8 = static_cast<const uint8_t*>(kv_fp8);
   p.kv_indptr = topk > 0 ? nullptr : kv_indptr;
   p.topk = topk;
   p.qo_indptr = prefill ? qo_indptr : nullptr;
@@ -266,9 +268,11 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   if (!ev) prof_lk.unlock();
   if (ev) cudaEventRecord(ev[0], stream);
   {
-    mla::TmaMaps maps;
-    st = build_maps(p, &maps);
-    if (st != MLA_OK) return st;
+    mla::TmaMaps maps{};
+    if (!kv_fp8) {  // an FP8 cache is read by copies only
+      st = build_maps(p, &maps);
+      if (st != MLA_OK) return st;
+    }
     // Small pages, or the scattered keys of sparse decode: the instance that copies
     // tiles slot by slot with two warps.
     const bool gather = dims->page_size % 64 != 0 || topk > 0;
@@ -313,6 +317,26 @@ int mla_paged_decode_sparse(const void* q_nope, const void* q_pe, const void* ck
   if (d.batch > 0 && !indices) return MLA_ERR_NULL;
   return run(false, 0, q_nope, q_pe, ckv_cache, kpe_cache, nullptr, nullptr, indices, sm_scale, out, lse, &d,
              workspace, workspace_bytes, flags, stream, topk);
+}
+
+int mla_paged_decode_fp8(const void* q_nope, const void* q_pe, const void* kv_fp8, const int32_t* kv_indptr,
+                         const int32_t* kv_indices, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                         void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  return run(false, 0, q_nope, q_pe, nullptr, nullptr, nullptr, kv_indptr, kv_indices, sm_scale, out, lse, dims,
+             workspace, workspace_bytes, flags, stream, 0, kv_fp8);
+}
+
+int mla_paged_decode_sparse_fp8(const void* q_nope, const void* q_pe, const void* kv_fp8, const int32_t* indices,
+                                int topk, float sm_scale, void* out, float* lse, const mla_dims* dims,
+                                void* workspace, size_t workspace_bytes, int flags, void* stream) {
+  if (!dims) return MLA_ERR_NULL;
+  if (topk < 1) return MLA_ERR_DIMS;
+  if ((long long)dims->batch * topk >= (1LL << 31)) return MLA_ERR_DIMS;
+  mla_dims d = *dims;
+  d.num_kv_indices = dims->batch * topk;
+  if (d.batch > 0 && !indices) return MLA_ERR_NULL;
+  return run(false, 0, q_nope, q_pe, nullptr, nullptr, nullptr, nullptr, indices, sm_scale, out, lse, &d,
+             workspace, workspace_bytes, flags, stream, topk, kv_fp8);
 }
 
 int mla_paged_prefill(const void* q_nope, const void* q_pe, const void* ckv_cache,

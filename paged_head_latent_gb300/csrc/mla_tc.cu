@@ -79,6 +79,7 @@ constexpr int kCopyWarp2 = 11;
 template <bool kGather, bool kPack>
 constexpr int instance_threads() { return kGather || !kPack ? 384 : 352; }
 constexpr int kStages = 4;
+constexpr int kFp8TokenBytes = 656;  // FP8 cache: 512 E4M3 + 4 float32 scales + 64 bf16
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kChunkPe = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
@@ -106,6 +107,33 @@ enum Bar : uint32_t {
   Q_FULL, KV_FULL0, KV_EMPTY0 = KV_FULL0 + kStages, S_FULL = KV_EMPTY0 + kStages, S_EMPTY, P_FULL, PV_DONE,
   X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, DESC0, NUM_BARS
 };
+
+// FP8 tile copy of one warp's 32 keys (keys k0 .. k0 + 31 of the tile, slot ids in lane
+// kk of sp): lane l loads 8 E4M3 latent bytes at lat + slot * 656 and the key's scale at
+// scl + slot * 656, all 32 keys' loads in flight, then stores the 8 scaled bf16 values
+// at row k of the chunk at dst_chunk (128-byte rows, 16-byte unit cu swizzled by k & 7).
+// A slot outside the cache gives zeros.  Not inlined: its 96 live registers would
+// otherwise crowd the whole kernel's allocation.
+static __device__ __noinline__ void fp8_copy_latent(const uint8_t* lat, const uint8_t* scl, int sp, int num_slots,
+                                                    uint32_t dst_chunk, int k0, uint32_t cu) {
+  uint2 raw[32];
+  float sc[32];
+#pragma unroll
+  for (int kk = 0; kk < 32; ++kk) {
+    const int slot = __shfl_sync(0xffffffffu, sp, kk);
+    const bool okk = slot >= 0 && slot < num_slots;
+    raw[kk] = okk ? ptx::ld_nc_v2(lat + (size_t)slot * kFp8TokenBytes) : make_uint2(0, 0);
+    sc[kk] = okk ? ptx::ld_nc_f32(scl + (size_t)slot * kFp8TokenBytes) : 0.f;
+  }
+#pragma unroll
+  for (int kk = 0; kk < 32; ++kk) {
+    const int k = k0 + kk;
+    const uint4 v = ptx::e4m3x8_scaled_to_bf16x8(raw[kk], sc[kk]);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst_chunk + k * 128 + ((cu ^ (k & 7)) << 4)),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+  }
+}
 
 // The two softmax warps that serve the same TMEM lanes (w and w + 4) meet at a named
 // barrier.  A warp leaves the softmax loop early only after some wait gave up, which
@@ -214,7 +242,7 @@ static_assert(sizeof(TileDesc) == 40, "descriptor size");
 // so tiles are copied slot by slot and the producer reads slot ids a tile ahead.
 // kPack: packed multi-token decode; TMEM lane m holds token m / mtp_h, head m % mtp_h of
 // the request, and each token's causal horizon masks the scores lane by lane.
-template <bool kGather, bool kPack>
+template <bool kGather, bool kPack, bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGather, kPack>(), 1)
     mla_tc_kernel(const __grid_constant__ TmaMaps maps, const MlaParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -291,7 +319,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
   if (warp == kProducerWarp || (kGather && warp == kCopyWarp2)) {
     const int part = kGather && warp == kCopyWarp2 ? 1 : 0;  // copy warp index
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (!kFp8 && lane == 0) {  // (an FP8 call builds no tensor maps)
       prefetch_tensormap(&maps.ckv);
       prefetch_tensormap(&maps.kpe);
     }
@@ -344,6 +372,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
         // Slot ids first, so their load overlaps the wait for a free stage.
         tile_slots(it.seg, it.t, s0, s1, contiguous, first, valid);
       }
+      if constexpr (kFp8) contiguous = false;  // an FP8 tile is always copied (dequantised)
       if (j >= kStages &&
           !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout, wait_ns))
         break;
@@ -414,7 +443,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
         const char* ckv_src = reinterpret_cast<const char*>(p.ckv + ckv_col) + lane * 16;
         const uint32_t cu = lane & 7, cc = lane >> 3;
         const char* kpe_src = reinterpret_cast<const char*>(p.kpe + kpe_col) + (lane & 3) * 16;
-        if constexpr (kGather) {  // this warp's 32 keys: part * 32 .. + 31
+        if constexpr (kFp8) {
+          // This warp's 32 keys.  Lane l dequantises latent values 8l .. 8l+7 of the
+          // CTA's half (token bytes 256*rank + 8l ..) with the key's scale of tile
+          // 2*rank + l/16 into the bf16 layout the copies above would write; every key's
+          // loads are issued before the first is converted.  The rope part is bf16 in the
+          // token (bytes 528 ..) and copied as usual.
+          constexpr size_t kTok = kFp8TokenBytes;
+          const int sp = part ? s1 : s0;
+          const uint8_t* lat = p.kv_fp8 + 256 * rank + 8 * lane;
+          const uint8_t* scl = p.kv_fp8 + 512 + 4 * (2 * rank + (lane >> 4));
+          fp8_copy_latent(lat, scl, sp, p.num_slots, dst + cc * kChunkKV, 32 * part, cu);
+          const uint8_t* rope = p.kv_fp8 + 528 + 64 * rank + (lane & 3) * 16;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kk = 8 * i + (lane >> 2), k = 32 * part + kk;
+            const int slot = __shfl_sync(0xffffffffu, sp, kk);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
+                              rope + (okk ? (size_t)slot * kTok : 0), okk ? 16 : 0);
+          }
+        } else if constexpr (kGather) {  // this warp's 32 keys: part * 32 .. + 31
           const int sp = part ? s1 : s0;
 #pragma unroll 8
           for (int kk = 0; kk < 32; ++kk) {
@@ -894,7 +943,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
 uint32_t tc_smem_bytes() { return kSmemBytes; }
 
 namespace {
-template <bool kGather, bool kPack>
+template <bool kGather, bool kPack, bool kFp8>
 cudaError_t launch_instance(const TmaMaps& maps, const MlaParams& p, cudaStream_t stream) {
   // The shared-memory attribute is set once per device and instance; calls may come from
   // any host thread.
@@ -906,21 +955,24 @@ cudaError_t launch_instance(const TmaMaps& maps, const MlaParams& p, cudaStream_
   {
     std::lock_guard<std::mutex> lk(mu);
     if (!configured[dev]) {
-      cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<kGather, kPack>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaError_t e = cudaFuncSetAttribute(mla_tc_kernel<kGather, kPack, kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)kSmemBytes);
       if (e != cudaSuccess) return e;
       configured[dev] = true;
     }
   }
-  mla_tc_kernel<kGather, kPack><<<2 * p.workers, instance_threads<kGather, kPack>(), kSmemBytes, stream>>>(maps, p);
+  mla_tc_kernel<kGather, kPack, kFp8><<<2 * p.workers, instance_threads<kGather, kPack>(), kSmemBytes, stream>>>(maps, p);
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_tc(const TmaMaps& maps, const MlaParams& p, bool gather, cudaStream_t stream) {
   const bool pack = p.mtp_q > 0;
-  if (gather) return pack ? launch_instance<true, true>(maps, p, stream) : launch_instance<true, false>(maps, p, stream);
-  return pack ? launch_instance<false, true>(maps, p, stream) : launch_instance<false, false>(maps, p, stream);
+  // An FP8 cache: every tile is copied and dequantised by the copy warps.
+  if (p.kv_fp8) return pack ? cudaErrorInvalidValue : launch_instance<true, false, true>(maps, p, stream);
+  if (gather)
+    return pack ? launch_instance<true, true, false>(maps, p, stream) : launch_instance<true, false, false>(maps, p, stream);
+  return pack ? launch_instance<false, true, false>(maps, p, stream) : launch_instance<false, false, false>(maps, p, stream);
 }
 
 }  // namespace mla

@@ -3,6 +3,8 @@
 // mbarrier wait, which gives up after kWaitTimeoutNs and raises the kernel's abort flag.
 #pragma once
 #include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace mla {
@@ -150,6 +152,37 @@ __device__ __forceinline__ void st_global_v4_hint(void* ptr, uint4 v, uint64_t p
 // 16) are zero-filled, so a zero-byte copy reads nothing and writes zeros.
 __device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+// Read-only 8-byte and 4-byte global loads (data no kernel of this call writes).
+__device__ __forceinline__ uint2 ld_nc_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float ld_nc_f32(const void* p) {
+  float v;
+  asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+// Eight E4M3 codes (bytes 0..7 of raw, in memory order) times `scale`, as eight bf16
+// in memory order: each code pair converts exactly to f16x2, each value widens exactly
+// to f32, the product is one f32 multiply (round to nearest even), and the pair is
+// rounded to bf16x2 (nearest even).
+__device__ __forceinline__ uint4 e4m3x8_scaled_to_bf16x8(uint2 raw, float scale) {
+  uint32_t o[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const uint16_t pair = static_cast<uint16_t>(((h < 2 ? raw.x : raw.y) >> (16 * (h & 1))) & 0xffffu);
+    uint32_t f16x2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+    const __half2 hh = *reinterpret_cast<const __half2*>(&f16x2);
+    const float lo = __low2float(hh) * scale, hi = __high2float(hh) * scale;
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    o[h] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // The barrier counts one more arrival, which happens when this thread's earlier

@@ -28,6 +28,11 @@ def np_inputs(w):
 def oracle_run(w, rows=None):
     import oracle
     a = np_inputs(w)
+    if w.kind == "decode_fp8":
+        return oracle.mla_decode_fp8(a["q_nope"], a["q_pe"], w.kv_fp8.numpy(), a["kv_indptr"], a["kv_indices"],
+                                     a["sm_scale"])
+    if w.kind == "sparse_fp8":
+        return oracle.mla_sparse_decode_fp8(a["q_nope"], a["q_pe"], w.kv_fp8.numpy(), a["indices"], a["sm_scale"])
     if w.kind == "sparse":
         return oracle.mla_sparse_decode(a["q_nope"], a["q_pe"], a["ckv_cache"], a["kpe_cache"], a["indices"],
                                         a["sm_scale"])
