@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA paged decode µs/call, KV TB/s & TFLOP/s as % of GB300 roofline"
 HEADLINE = "decode_b128_h128_ps1"
 SUB_WORKLOADS = ("decode_b4_h16_ps64", "decode_b64_h128_ps64", "decode_b32_h128_skew", "prefill_causal_h128",
-                 "mtp_b64_h16_q4_ps64", "sparse_b64_h128_topk2048")
+                 "mtp_b64_h16_q4_ps64", "sparse_b64_h128_topk2048", "fp8_b64_h128_ps64")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 256 << 20
 
@@ -56,21 +56,25 @@ def algorithmic_work(w):
     its keys, so each is read once); 1152 B q + 1024 B out + 4 B lse per (row, head);
     2 * (576 + 512) flops per (visible key, head), a visible key being a (query row, key)
     pair that the causal mask keeps.  Sparse decode: 1152 B per valid entry (padding
-    entries read only their 4 B index)."""
+    entries read only their 4 B index).  An FP8 cache holds 656 B per key instead of 1152."""
     keys = w.visible_keys()
     rows_heads = w.rows * w.num_qo_heads
-    if w.kind == "sparse":
-        nbytes = keys * 1152 + w.num_kv_indices * 4 + rows_heads * (1152 + 1024 + 4)
+    kv_bytes = 656 if w.kind.endswith("_fp8") else 1152
+    if w.kind.startswith("sparse"):
+        nbytes = keys * kv_bytes + w.num_kv_indices * 4 + rows_heads * (1152 + 1024 + 4)
     else:
-        nbytes = sum(w.kv_lens()) * (1152 + 4) + rows_heads * (1152 + 1024 + 4)
+        nbytes = sum(w.kv_lens()) * (kv_bytes + 4) + rows_heads * (1152 + 1024 + 4)
     flops = keys * w.num_qo_heads * 2 * (576 + 512)
     return nbytes, flops, keys
 
 
 def config_of(w):
     """The workload description both arms print (identical keys and values)."""
-    return {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads, "page_size": w.page_size,
-            "visible_keys": w.visible_keys()}
+    c = {"workload": w.name, "batch": w.batch, "num_qo_heads": w.num_qo_heads, "page_size": w.page_size,
+         "visible_keys": w.visible_keys()}
+    if w.kv_fp8 is not None:
+        c["kv_cache"] = "fp8 e4m3 latent + fp32 tile scales + bf16 rope, 656 B/token"
+    return c
 
 
 # The sources that define the attention kernel; the recorded DRAM traffic is valid only
@@ -186,8 +190,11 @@ def time_oracle(w, budget_s, max_rows=None):
         r, k0, n = rows[k]
         slots = w.kv_indices[k0:k0 + max(n, 0)].long()
         slots = slots[(slots >= 0) & (slots < ckv.shape[0])]  # sparse decode: padding entries are skipped
-        oracle.attend(w.q_nope[r].float().numpy(), w.q_pe[r].float().numpy(), ckv[slots].float().numpy(),
-                      kpe[slots].float().numpy(), w.sm_scale)
+        if w.kv_fp8 is not None:  # the FP8 oracle reads the row's tokens back to BF16 first
+            k_ckv, k_kpe = oracle.dequantize_fp8_cache(w.kv_fp8.view(-1, 656)[slots].numpy())
+        else:
+            k_ckv, k_kpe = ckv[slots].float().numpy(), kpe[slots].float().numpy()
+        oracle.attend(w.q_nope[r].float().numpy(), w.q_pe[r].float().numpy(), k_ckv, k_kpe, w.sm_scale)
         keys += slots.numel()
         done += 1
         if time.perf_counter() - t0 >= budget_s or (max_rows and done >= max_rows):

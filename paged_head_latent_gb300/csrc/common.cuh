@@ -57,6 +57,8 @@ struct MlaParams {
   const uint8_t* kv_fp8;
 };
 
+constexpr int kFp8TokenBytes = 656;  // FP8 cache: 512 E4M3 + 4 float32 scales + 64 bf16 per token
+
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout: [status (256 B)] [records: G x 24 B] [merge counters] [part_lse] [part_o].

@@ -109,10 +109,10 @@ struct MapKey {
   const void* ptr;
   uint64_t rows, cols;
   uint32_t box_cols, box_rows;
-  int swizzle, promo;
+  int swizzle, promo, bytes;  // bytes: element size (2: bf16, 1: uint8)
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && rows == o.rows && cols == o.cols && box_cols == o.box_cols && box_rows == o.box_rows &&
-           swizzle == o.swizzle && promo == o.promo;
+           swizzle == o.swizzle && promo == o.promo && bytes == o.bytes;
   }
 };
 
@@ -121,14 +121,15 @@ struct MapCache {
   std::vector<std::pair<MapKey, CUtensorMap>> entries;  // most recent last
 } g_maps;
 
-// 2-D bf16 map over [rows, cols] (row stride = cols), box = box_cols x box_rows.
+// 2-D map over [rows, cols] of bf16 (bytes = 2) or uint8 (bytes = 1) elements (row
+// stride = cols elements), box = box_cols x box_rows.
 int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows,
-            CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo) {
+            CUtensorMapSwizzle swizzle, CUtensorMapL2promotion promo, int bytes = 2) {
   if (rows == 0) {  // nothing can be loaded: the kernel is given no keys / rows for it
     std::memset(out, 0, sizeof(*out));
     return MLA_OK;
   }
-  const MapKey key{ptr, rows, cols, box_cols, box_rows, (int)swizzle, (int)promo};
+  const MapKey key{ptr, rows, cols, box_cols, box_rows, (int)swizzle, (int)promo, bytes};
   std::lock_guard<std::mutex> lk(g_maps.mu);
   for (auto& e : g_maps.entries)
     if (e.first == key) {
@@ -139,11 +140,12 @@ int get_map(CUtensorMap* out, const void* ptr, uint64_t rows, uint64_t cols, uin
   if (!fn) return MLA_ERR_CUDA;
   alignas(64) CUtensorMap m;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
+  cuuint64_t strides[1] = {cols * (cuuint64_t)bytes};
   cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = fn(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const auto dt = bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  CUresult r = fn(&m, dt, 2, const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return MLA_ERR_CUDA;
   if (g_maps.entries.size() >= 96) g_maps.entries.erase(g_maps.entries.begin());
   g_maps.entries.emplace_back(key, m);
@@ -161,6 +163,22 @@ int build_maps(const MlaParams& p, mla::TmaMaps* m) {
   int st;
   if ((st = get_map(&m->ckv, p.ckv, slots, 512, 64, 64, sw128, l256)) != MLA_OK) return st;
   if ((st = get_map(&m->kpe, p.kpe, slots, 64, 32, 64, sw64, l128)) != MLA_OK) return st;
+  return MLA_OK;
+}
+
+// The FP8 cache's maps, over its tokens as [slots, 656] bytes (a whole run of 64 slots
+// per tile): the latent half of a CTA in boxes of 16 tokens x 256 bytes, the four scales
+// in boxes of 32 tokens x 16 bytes, and the rope half in a box of 64 tokens x 64 bytes
+// with the 64-byte swizzle the bf16 kpe tiles have.
+int build_fp8_maps(const MlaParams& p, mla::TmaMaps* m) {
+  const uint64_t slots = (uint64_t)p.num_slots;
+  const auto none = CU_TENSOR_MAP_SWIZZLE_NONE, sw64 = CU_TENSOR_MAP_SWIZZLE_64B;
+  const auto l256 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B, l128 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
+  const uint64_t tok = mla::kFp8TokenBytes;
+  int st;
+  if ((st = get_map(&m->f8_lat, p.kv_fp8, slots, tok, 256, 16, none, l256, 1)) != MLA_OK) return st;
+  if ((st = get_map(&m->f8_scl, p.kv_fp8, slots, tok, 16, 32, none, l128, 1)) != MLA_OK) return st;
+  if ((st = get_map(&m->f8_rope, p.kv_fp8, slots, tok, 64, 64, sw64, l128, 1)) != MLA_OK) return st;
   return MLA_OK;
 }
 
@@ -269,10 +287,8 @@ int run(bool prefill, int q_len, const void* q_nope, const void* q_pe, const voi
   if (ev) cudaEventRecord(ev[0], stream);
   {
     mla::TmaMaps maps{};
-    if (!kv_fp8) {  // an FP8 cache is read by copies only
-      st = build_maps(p, &maps);
-      if (st != MLA_OK) return st;
-    }
+    st = kv_fp8 ? build_fp8_maps(p, &maps) : build_maps(p, &maps);
+    if (st != MLA_OK) return st;
     // Small pages, or the scattered keys of sparse decode: the instance that copies
     // tiles slot by slot with two warps.
     const bool gather = dims->page_size % 64 != 0 || topk > 0;

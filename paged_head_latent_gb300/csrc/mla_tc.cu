@@ -79,7 +79,6 @@ constexpr int kCopyWarp2 = 11;
 template <bool kGather, bool kPack>
 constexpr int instance_threads() { return kGather || !kPack ? 384 : 352; }
 constexpr int kStages = 4;
-constexpr int kFp8TokenBytes = 656;  // FP8 cache: 512 E4M3 + 4 float32 scales + 64 bf16
 constexpr int kQkSteps = 18;                // 288-wide depth slice / 16
 constexpr uint32_t kChunkKV = 64 * 128;     // 64 rows x 64 bf16, 128-byte swizzle
 constexpr uint32_t kChunkPe = 64 * 64;      // 64 rows x 32 bf16, 64-byte swizzle
@@ -105,26 +104,17 @@ constexpr float kRescaleLog2 = 8.0f;  // rescale O only when the max grows by mo
 
 enum Bar : uint32_t {
   Q_FULL, KV_FULL0, KV_EMPTY0 = KV_FULL0 + kStages, S_FULL = KV_EMPTY0 + kStages, S_EMPTY, P_FULL, PV_DONE,
-  X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, DESC0, NUM_BARS
+  X_FULL0, O_FULL = X_FULL0 + 16, O_EMPTY, DRAIN, DESC0,
+  RAW0,  // FP8 instance: a stage's raw bytes have landed (one per stage)
+  NUM_BARS = RAW0 + kStages
 };
 
-// FP8 tile copy of one warp's 32 keys (keys k0 .. k0 + 31 of the tile, slot ids in lane
-// kk of sp): lane l loads 8 E4M3 latent bytes at lat + slot * 656 and the key's scale at
-// scl + slot * 656, all 32 keys' loads in flight, then stores the 8 scaled bf16 values
-// at row k of the chunk at dst_chunk (128-byte rows, 16-byte unit cu swizzled by k & 7).
-// A slot outside the cache gives zeros.  Not inlined: its 96 live registers would
-// otherwise crowd the whole kernel's allocation.
-static __device__ __noinline__ void fp8_copy_latent(const uint8_t* lat, const uint8_t* scl, int sp, int num_slots,
-                                                    uint32_t dst_chunk, int k0, uint32_t cu) {
-  uint2 raw[32];
-  float sc[32];
-#pragma unroll
-  for (int kk = 0; kk < 32; ++kk) {
-    const int slot = __shfl_sync(0xffffffffu, sp, kk);
-    const bool okk = slot >= 0 && slot < num_slots;
-    raw[kk] = okk ? ptx::ld_nc_v2(lat + (size_t)slot * kFp8TokenBytes) : make_uint2(0, 0);
-    sc[kk] = okk ? ptx::ld_nc_f32(scl + (size_t)slot * kFp8TokenBytes) : 0.f;
-  }
+// Dequantised FP8 latent values of one warp's 32 keys (keys k0 .. k0 + 31 of the tile):
+// lane l holds each key's 8 E4M3 codes raw[kk] and its scale sc[kk] and stores the 8
+// scaled bf16 values at row k of the chunk at dst_chunk (128-byte rows, 16-byte unit cu
+// swizzled by k & 7), the layout the bf16 copies write.
+__device__ __forceinline__ void fp8_store_latent(const uint2 (&raw)[32], const float (&sc)[32], uint32_t dst_chunk,
+                                                 int k0, uint32_t cu) {
 #pragma unroll
   for (int kk = 0; kk < 32; ++kk) {
     const int k = k0 + kk;
@@ -274,6 +264,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
     mbar_init(bar(O_EMPTY), kSoftmaxWarps);
     mbar_init(bar(DRAIN), 2);  // one commit from each MMA-issuing thread
     mbar_init(bar(DESC0), 1);  // the first tile's descriptor is written
+    if (kFp8)
+      for (int s = 0; s < kStages; ++s) mbar_init(bar(RAW0 + s), 2);  // one arrival per copy warp
     fence_mbar_init();
     // Arm the first phase of every exchange barrier before the peer can send.
     for (int i = 0; i < 16; ++i) mbar_arrive_expect_tx(bar(X_FULL0 + i), kXWarpBytes);
@@ -319,9 +311,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
   if (warp == kProducerWarp || (kGather && warp == kCopyWarp2)) {
     const int part = kGather && warp == kCopyWarp2 ? 1 : 0;  // copy warp index
     // ------------------------------------------------------------ TMA producer
-    if (!kFp8 && lane == 0) {  // (an FP8 call builds no tensor maps)
-      prefetch_tensormap(&maps.ckv);
-      prefetch_tensormap(&maps.kpe);
+    if (lane == 0) {
+      if constexpr (kFp8) {
+        prefetch_tensormap(&maps.f8_lat);
+        prefetch_tensormap(&maps.f8_scl);
+        prefetch_tensormap(&maps.f8_rope);
+      } else {
+        prefetch_tensormap(&maps.ckv);
+        prefetch_tensormap(&maps.kpe);
+      }
     }
     // Slot ids of tile t of a segment: lanes hold keys lane and lane + 32; keys past
     // the row's length get a slot outside the cache (TMA reads zeros there).  A TMA tile
@@ -358,6 +356,162 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
     uint32_t j = 0;
     bool have_next = false;  // next_s0/next_s1 hold this tile's ids, loaded a tile ago
     int next_s0 = 0, next_s1 = 0;
+    if constexpr (kFp8) {
+      // ---- FP8 cache.  Copy warps 8 and 11 (part 0 / 1) each own 32 keys of every tile.
+      // For tile j a warp issues the tile's raw bytes into the stage as staging -- TMA
+      // boxes for a run of 64 slots (latent halves, scales, and the rope half straight to
+      // its place), cp.async otherwise -- then dequantises tile j - 1 from its staging into
+      // the bf16 layout the MMA reads: one tile of lag keeps a tile's loads in flight while
+      // the previous one is converted.  A warp's staging lies inside the rows it writes
+      // (half `part` of every 8 KB chunk: the latent of its keys 16h .. 16h + 15 in chunk
+      // 2 + h, their four scales each in chunk 0), and it reads all of it into registers
+      // before writing, so the two warps never wait for each other.
+      const uint32_t half_off = (uint32_t)part * 4096u;
+      auto stage_addr = [&](uint32_t t) { return sbase + kOffKV + (t % kStages) * kStageBytes; };
+      auto convert = [&](uint32_t t) -> bool {
+        if (!mbar_wait(bar(RAW0 + t % kStages), (t / kStages) & 1, abort, p.status, kStatusTimeout, wait_ns))
+          return false;
+        const uint32_t S = stage_addr(t);
+        uint2 raw[32];
+        float sc[32];
+#pragma unroll
+        for (int kk = 0; kk < 32; ++kk) {
+          const uint32_t la = S + (2 + (kk >> 4)) * kChunkKV + half_off + (kk & 15) * 256 + 8 * lane;
+          const uint32_t sa = S + half_off + kk * 16 + 4 * (2 * rank + (lane >> 4));
+          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(raw[kk].x), "=r"(raw[kk].y) : "r"(la) : "memory");
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sc[kk]) : "r"(sa) : "memory");
+        }
+        __syncwarp();
+        fp8_store_latent(raw, sc, S + (uint32_t)(lane >> 3) * kChunkKV, 32 * part, lane & 7);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(KV_FULL0 + t % kStages));  // (release: orders the stores)
+        return true;
+      };
+      uint32_t issued = 0;  // tiles whose raw bytes were requested
+      bool fok = true;
+      for (; it.live; it.advance(), ++j) {
+        const int stage = j % kStages;
+        int s0, s1, first;
+        bool contiguous;
+        unsigned long long valid;
+        if (have_next) {
+          s0 = next_s0;
+          s1 = next_s1;
+          eval_slots(min(kTileKeys, it.seg.len - it.t * kTileKeys), s0, s1, contiguous, first, valid);
+          have_next = false;
+        } else {
+          tile_slots(it.seg, it.t, s0, s1, contiguous, first, valid);
+        }
+        if (j >= kStages &&
+            !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout, wait_ns)) {
+          fok = false;
+          break;
+        }
+        const uint32_t S = stage_addr(j);
+        const uint32_t rawbar = bar(RAW0 + stage);
+        const bool skip = fault_worker && (int)j == p.fault_skip_tile;
+        if (lane == 0 && part == 0) {
+          TileDesc d;
+          d.t = it.t;
+          d.len = it.seg.len;
+          d.row = it.seg.row;
+          d.slot = it.seg.slot;
+          d.nseg = it.nseg;
+          d.flags = (it.first() ? kFirst : 0) | (it.last() ? kLast : 0) | (it.seg.whole ? kWhole : 0) | kCopied;
+          d.next_row = -1;
+          d.pad = 0;
+          d.valid = valid;
+          if (it.last()) {
+            TileIter peek = it;
+            peek.advance();
+            if (peek.live) {
+              d.next_row = peek.seg.row;
+              const size_t r = (size_t)d.next_row * p.heads;
+              if (rank == 0) bulk_prefetch_l2(p.q_nope + r * kDimCkv, p.heads * kDimCkv * 2);
+              else bulk_prefetch_l2(p.q_pe + r * kDimKpe, p.heads * kDimKpe * 2);
+            }
+          }
+          desc[j % kDescRing] = d;
+          if (j == 0) mbar_arrive(bar(DESC0));
+        }
+        __syncwarp();
+        if (skip) {
+          // Test of the give-up path: this tile's bytes are never requested.
+        } else if (contiguous) {
+          if (lane == 0) {
+            if (part == 0) {
+              fence_proxy_async_smem();  // the stage last held bf16 written by the generic proxy
+              mbar_arrive_expect_tx(rawbar, 4 * 4096 + 2 * 512 + 64 * 64);
+#pragma unroll
+              for (int g = 0; g < 4; ++g)  // keys 16g .. 16g + 15: part g / 2, chunk 2 + g % 2
+                tma_load_2d(S + (2 + (g & 1)) * kChunkKV + (g >> 1) * 4096, &maps.f8_lat, 256 * (int)rank,
+                                 first + 16 * g, rawbar);
+#pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_2d(S + h * 4096, &maps.f8_scl, 512, first + 32 * h, rawbar);
+              tma_load_2d(S + 4 * kChunkKV, &maps.f8_rope, 528 + 64 * (int)rank, first, rawbar);
+            } else {
+              mbar_arrive(rawbar);
+            }
+          }
+        } else {
+          if (!it.last()) {  // the next tile of this row: its slot ids a tile ahead
+            const int key1 = (it.t + 1) * kTileKeys;
+            const int nv1 = min(kTileKeys, it.seg.len - key1);
+            const int* ip1 = p.kv_indices + it.seg.kv0 + key1;
+            next_s0 = lane < nv1 ? __ldg(ip1 + lane) : p.num_slots;
+            next_s1 = lane + 32 < nv1 ? __ldg(ip1 + lane + 32) : p.num_slots;
+            have_next = true;
+          }
+          const int sp = part ? s1 : s0;
+          const uint8_t* tok = p.kv_fp8;
+#pragma unroll 4
+          for (int i = 0; i < 16; ++i) {  // two keys per instruction: 16 lanes x 16 bytes each
+            const int kk = 2 * i + (lane >> 4);
+            const int slot = __shfl_sync(0xffffffffu, sp, kk);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(S + (2 + (kk >> 4)) * kChunkKV + half_off + (kk & 15) * 256 + 16 * (lane & 15),
+                              tok + (okk ? (size_t)slot * kFp8TokenBytes + 256 * rank + 16 * (lane & 15) : 0),
+                              okk ? 16 : 0);
+          }
+          {  // the four scales of key `lane`
+            const bool okk = sp >= 0 && sp < p.num_slots;
+            cp_async_16_zfill(S + half_off + lane * 16, tok + (okk ? (size_t)sp * kFp8TokenBytes + 512 : 0),
+                              okk ? 16 : 0);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {  // the rope half, into its place
+            const int kk = 8 * i + (lane >> 2), k = 32 * part + kk;
+            const int slot = __shfl_sync(0xffffffffu, sp, kk);
+            const bool okk = slot >= 0 && slot < p.num_slots;
+            cp_async_16_zfill(S + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
+                              tok + (okk ? (size_t)slot * kFp8TokenBytes + 528 + 64 * rank + (lane & 3) * 16 : 0),
+                              okk ? 16 : 0);
+          }
+          cp_async_mbar_arrive(rawbar);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(rawbar);
+        }
+        __syncwarp();
+        issued = j + 1;
+        if (j >= 1 && !convert(j - 1)) {
+          fok = false;
+          break;
+        }
+      }
+      if (fok && issued >= 1) convert(issued - 1);
+      // Drain: wait (bounded) for the last raw request of every stage, so no copy is in
+      // flight when the CTA exits, whatever happened above.
+      if (lane == 0) {
+        volatile int no_abort = 0;
+        for (uint32_t s = 0; s < kStages && s < issued; ++s) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % kStages);
+          if (fault_worker && (int)last == p.fault_skip_tile) continue;  // never requested
+          mbar_wait(bar(RAW0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout,
+                    wait_ns);
+        }
+      }
+    } else {
     for (; it.live; it.advance(), ++j) {
       const int stage = j % kStages;
       int s0, s1, first;
@@ -372,7 +526,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
         // Slot ids first, so their load overlaps the wait for a free stage.
         tile_slots(it.seg, it.t, s0, s1, contiguous, first, valid);
       }
-      if constexpr (kFp8) contiguous = false;  // an FP8 tile is always copied (dequantised)
       if (j >= kStages &&
           !mbar_wait(bar(KV_EMPTY0 + stage), ((j / kStages) - 1) & 1, abort, p.status, kStatusTimeout, wait_ns))
         break;
@@ -443,27 +596,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
         const char* ckv_src = reinterpret_cast<const char*>(p.ckv + ckv_col) + lane * 16;
         const uint32_t cu = lane & 7, cc = lane >> 3;
         const char* kpe_src = reinterpret_cast<const char*>(p.kpe + kpe_col) + (lane & 3) * 16;
-        if constexpr (kFp8) {
-          // This warp's 32 keys.  Lane l dequantises latent values 8l .. 8l+7 of the
-          // CTA's half (token bytes 256*rank + 8l ..) with the key's scale of tile
-          // 2*rank + l/16 into the bf16 layout the copies above would write; every key's
-          // loads are issued before the first is converted.  The rope part is bf16 in the
-          // token (bytes 528 ..) and copied as usual.
-          constexpr size_t kTok = kFp8TokenBytes;
-          const int sp = part ? s1 : s0;
-          const uint8_t* lat = p.kv_fp8 + 256 * rank + 8 * lane;
-          const uint8_t* scl = p.kv_fp8 + 512 + 4 * (2 * rank + (lane >> 4));
-          fp8_copy_latent(lat, scl, sp, p.num_slots, dst + cc * kChunkKV, 32 * part, cu);
-          const uint8_t* rope = p.kv_fp8 + 528 + 64 * rank + (lane & 3) * 16;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int kk = 8 * i + (lane >> 2), k = 32 * part + kk;
-            const int slot = __shfl_sync(0xffffffffu, sp, kk);
-            const bool okk = slot >= 0 && slot < p.num_slots;
-            cp_async_16_zfill(dst + 4 * kChunkKV + k * 64 + (((lane & 3) ^ ((k >> 1) & 3)) << 4),
-                              rope + (okk ? (size_t)slot * kTok : 0), okk ? 16 : 0);
-          }
-        } else if constexpr (kGather) {  // this warp's 32 keys: part * 32 .. + 31
+        if constexpr (kGather) {  // this warp's 32 keys: part * 32 .. + 31
           const int sp = part ? s1 : s0;
 #pragma unroll 8
           for (int kk = 0; kk < 32; ++kk) {
@@ -514,6 +647,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
         mbar_wait(bar(KV_FULL0 + (last % kStages)), (last / kStages) & 1, &no_abort, p.status, kStatusTimeout, wait_ns);
       }
     }
+    }  // bf16 caches
   } else if (warp == kMmaWarp || warp == kPvWarp) {
     // ------------------------------------------------------------ MMA issuers
     // tcgen05.mma issue blocks while the tensor pipe is busy, so QK and PV come from

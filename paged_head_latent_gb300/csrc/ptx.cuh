@@ -168,8 +168,8 @@ __device__ __forceinline__ float ld_nc_f32(const void* p) {
 
 // Eight E4M3 codes (bytes 0..7 of raw, in memory order) times `scale`, as eight bf16
 // in memory order: each code pair converts exactly to f16x2, each value widens exactly
-// to f32, the product is one f32 multiply (round to nearest even), and the pair is
-// rounded to bf16x2 (nearest even).
+// to f32, the pair's products are one packed f32x2 multiply (each rounded to nearest
+// even, as a scalar multiply would), and the pair is rounded to bf16x2 (nearest even).
 __device__ __forceinline__ uint4 e4m3x8_scaled_to_bf16x8(uint2 raw, float scale) {
   uint32_t o[4];
 #pragma unroll
@@ -178,7 +178,13 @@ __device__ __forceinline__ uint4 e4m3x8_scaled_to_bf16x8(uint2 raw, float scale)
     uint32_t f16x2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
     const __half2 hh = *reinterpret_cast<const __half2*>(&f16x2);
-    const float lo = __low2float(hh) * scale, hi = __high2float(hh) * scale;
+    const float a0 = __low2float(hh), a1 = __high2float(hh);
+    unsigned long long in, sc2, prod;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(in) : "f"(a0), "f"(a1));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(sc2) : "f"(scale));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(prod) : "l"(in), "l"(sc2));
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(prod));
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     o[h] = *reinterpret_cast<const uint32_t*>(&b);
   }

@@ -27,10 +27,20 @@ def test_inject_hook_rejects_bad_arguments(lib):
     assert lib.lib().mla_debug_inject_timeout(-1, 0) == 0
 
 
+CASES = {
+    "bf16": lambda: wl.make_decode([1000, 300], num_qo_heads=16, page_size=64, seed=4000),
+    # FP8 caches have their own producer: raw bytes by TMA boxes (page 64) or cp.async
+    # (page 16), converted a tile later, with its own give-up and drain path.
+    "fp8_tma": lambda: wl.quantize_fp8(wl.make_decode([1000, 300], num_qo_heads=16, page_size=64, seed=4001)),
+    "fp8_copy": lambda: wl.quantize_fp8(wl.make_decode([1000, 300], num_qo_heads=16, page_size=16, seed=4002)),
+}
+
+
 @pytest.mark.gpu
-def test_bounded_wait_gives_up_and_reports_timeout(lib):
+@pytest.mark.parametrize("case", sorted(CASES))
+def test_bounded_wait_gives_up_and_reports_timeout(lib, case):
     require_gpu()
-    w_cpu = wl.make_decode([1000, 300], num_qo_heads=16, page_size=64, seed=4000)
+    w_cpu = CASES[case]()
     w = w_cpu.to("cuda")
     ws = torch.zeros(lib.workload_workspace_bytes(w, 1), dtype=torch.uint8, device="cuda")
     assert lib.lib().mla_debug_inject_timeout(2, 2_000_000) == 0
