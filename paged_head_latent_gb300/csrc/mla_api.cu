@@ -167,7 +167,7 @@ int build_maps(const MlaParams& p, mla::TmaMaps* m) {
 }
 
 // The FP8 cache's maps, over its tokens as [slots, 656] bytes (a whole run of 64 slots
-// per tile): the latent half of a CTA in boxes of 16 tokens x 256 bytes, the four scales
+// per tile): the latent half of a CTA in two boxes of 64 tokens x 128 bytes, the four scales
 // in boxes of 32 tokens x 16 bytes, and the rope half in a box of 64 tokens x 64 bytes
 // with the 64-byte swizzle the bf16 kpe tiles have.
 int build_fp8_maps(const MlaParams& p, mla::TmaMaps* m) {
@@ -176,7 +176,7 @@ int build_fp8_maps(const MlaParams& p, mla::TmaMaps* m) {
   const auto l256 = CU_TENSOR_MAP_L2_PROMOTION_L2_256B, l128 = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;
   const uint64_t tok = mla::kFp8TokenBytes;
   int st;
-  if ((st = get_map(&m->f8_lat, p.kv_fp8, slots, tok, 256, 16, none, l256, 1)) != MLA_OK) return st;
+  if ((st = get_map(&m->f8_lat, p.kv_fp8, slots, tok, 128, 64, none, l256, 1)) != MLA_OK) return st;
   if ((st = get_map(&m->f8_scl, p.kv_fp8, slots, tok, 16, 32, none, l128, 1)) != MLA_OK) return st;
   if ((st = get_map(&m->f8_rope, p.kv_fp8, slots, tok, 64, 64, sw64, l128, 1)) != MLA_OK) return st;
   return MLA_OK;

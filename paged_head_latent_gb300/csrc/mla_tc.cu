@@ -109,16 +109,16 @@ enum Bar : uint32_t {
   NUM_BARS = RAW0 + kStages
 };
 
-// Dequantised FP8 latent values of one warp's 32 keys (keys k0 .. k0 + 31 of the tile):
-// lane l holds each key's 8 E4M3 codes raw[kk] and its scale sc[kk] and stores the 8
-// scaled bf16 values at row k of the chunk at dst_chunk (128-byte rows, 16-byte unit cu
-// swizzled by k & 7), the layout the bf16 copies write.
-__device__ __forceinline__ void fp8_store_latent(const uint2 (&raw)[32], const float (&sc)[32], uint32_t dst_chunk,
+// Dequantised FP8 latent values of 8 keys (keys k0 .. k0 + 7 of the tile): lane l holds
+// each key's 8 E4M3 codes raw[i] and its scale sc[i] and stores the 8 scaled bf16 values
+// at row k of the chunk at dst_chunk (128-byte rows, 16-byte unit cu swizzled by k & 7),
+// the layout the bf16 copies write.
+__device__ __forceinline__ void fp8_store_latent(const uint2 (&raw)[8], const float (&sc)[8], uint32_t dst_chunk,
                                                  int k0, uint32_t cu) {
 #pragma unroll
-  for (int kk = 0; kk < 32; ++kk) {
-    const int k = k0 + kk;
-    const uint4 v = ptx::e4m3x8_scaled_to_bf16x8(raw[kk], sc[kk]);
+  for (int i = 0; i < 8; ++i) {
+    const int k = k0 + i;
+    const uint4 v = ptx::e4m3x8_scaled_to_bf16x8(raw[i], sc[i]);
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst_chunk + k * 128 + ((cu ^ (k & 7)) << 4)),
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
@@ -363,26 +363,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
       // its place), cp.async otherwise -- then dequantises tile j - 1 from its staging into
       // the bf16 layout the MMA reads: one tile of lag keeps a tile's loads in flight while
       // the previous one is converted.  A warp's staging lies inside the rows it writes
-      // (half `part` of every 8 KB chunk: the latent of its keys 16h .. 16h + 15 in chunk
-      // 2 + h, their four scales each in chunk 0), and it reads all of it into registers
-      // before writing, so the two warps never wait for each other.
+      // (half `part` of every 8 KB chunk): the two 128-byte halves of key k's latent sit in
+      // row k of chunks 2 and 3 -- the rows key k's bf16 values replace -- and the warp's
+      // 32 keys' scales in its rows 24 .. 27 of chunk 1, which only the last group of keys
+      // overwrites.  Converting 8 keys at a time (group g writes rows 8g .. 8g + 7) thus
+      // never overwrites staging it has not read, and the two warps never wait for each
+      // other.
       const uint32_t half_off = (uint32_t)part * 4096u;
       auto stage_addr = [&](uint32_t t) { return sbase + kOffKV + (t % kStages) * kStageBytes; };
       auto convert = [&](uint32_t t) -> bool {
         if (!mbar_wait(bar(RAW0 + t % kStages), (t / kStages) & 1, abort, p.status, kStatusTimeout, wait_ns))
           return false;
         const uint32_t S = stage_addr(t);
-        uint2 raw[32];
-        float sc[32];
+        // Lane l's 8 codes of key kk: latent bytes 8l .. 8l + 7, in chunk 2 + l / 16.
+        const uint32_t lat_s = S + (2 + (lane >> 4)) * kChunkKV + half_off + 8 * (lane & 15);
+        const uint32_t scl_s = S + kChunkKV + half_off + 3072 + 4 * (2 * rank + (lane >> 4));
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
+          uint2 raw[8];
+          float sc[8];
 #pragma unroll
-        for (int kk = 0; kk < 32; ++kk) {
-          const uint32_t la = S + (2 + (kk >> 4)) * kChunkKV + half_off + (kk & 15) * 256 + 8 * lane;
-          const uint32_t sa = S + half_off + kk * 16 + 4 * (2 * rank + (lane >> 4));
-          asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(raw[kk].x), "=r"(raw[kk].y) : "r"(la) : "memory");
-          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sc[kk]) : "r"(sa) : "memory");
+          for (int i = 0; i < 8; ++i) {
+            const int kk = 8 * g + i;
+            asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(raw[i].x), "=r"(raw[i].y) : "r"(lat_s + kk * 128)
+                         : "memory");
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sc[i]) : "r"(scl_s + kk * 16) : "memory");
+          }
+          __syncwarp();
+          fp8_store_latent(raw, sc, S + (uint32_t)(lane >> 3) * kChunkKV, 32 * part + 8 * g, lane & 7);
         }
-        __syncwarp();
-        fp8_store_latent(raw, sc, S + (uint32_t)(lane >> 3) * kChunkKV, 32 * part, lane & 7);
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(KV_FULL0 + t % kStages));  // (release: orders the stores)
         return true;
@@ -441,14 +450,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
           if (lane == 0) {
             if (part == 0) {
               fence_proxy_async_smem();  // the stage last held bf16 written by the generic proxy
-              mbar_arrive_expect_tx(rawbar, 4 * 4096 + 2 * 512 + 64 * 64);
+              mbar_arrive_expect_tx(rawbar, 2 * 8192 + 2 * 512 + 64 * 64);
 #pragma unroll
-              for (int g = 0; g < 4; ++g)  // keys 16g .. 16g + 15: part g / 2, chunk 2 + g % 2
-                tma_load_2d(S + (2 + (g & 1)) * kChunkKV + (g >> 1) * 4096, &maps.f8_lat, 256 * (int)rank,
-                                 first + 16 * g, rawbar);
+              for (int h = 0; h < 2; ++h)  // latent bytes 128h .. 128h + 127 of the CTA's half: chunk 2 + h
+                tma_load_2d(S + (2 + h) * kChunkKV, &maps.f8_lat, 256 * (int)rank + 128 * h, first, rawbar);
 #pragma unroll
-              for (int h = 0; h < 2; ++h)
-                tma_load_2d(S + h * 4096, &maps.f8_scl, 512, first + 32 * h, rawbar);
+              for (int h = 0; h < 2; ++h)  // scales of keys 32h .. 32h + 31: chunk 1, rows 32h + 24 ..
+                tma_load_2d(S + kChunkKV + h * 4096 + 3072, &maps.f8_scl, 512, first + 32 * h, rawbar);
               tma_load_2d(S + 4 * kChunkKV, &maps.f8_rope, 528 + 64 * (int)rank, first, rawbar);
             } else {
               mbar_arrive(rawbar);
@@ -470,13 +478,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(instance_threads<kGa
             const int kk = 2 * i + (lane >> 4);
             const int slot = __shfl_sync(0xffffffffu, sp, kk);
             const bool okk = slot >= 0 && slot < p.num_slots;
-            cp_async_16_zfill(S + (2 + (kk >> 4)) * kChunkKV + half_off + (kk & 15) * 256 + 16 * (lane & 15),
+            cp_async_16_zfill(S + (2 + ((lane & 15) >> 3)) * kChunkKV + half_off + kk * 128 + 16 * (lane & 7),
                               tok + (okk ? (size_t)slot * kFp8TokenBytes + 256 * rank + 16 * (lane & 15) : 0),
                               okk ? 16 : 0);
           }
           {  // the four scales of key `lane`
             const bool okk = sp >= 0 && sp < p.num_slots;
-            cp_async_16_zfill(S + half_off + lane * 16, tok + (okk ? (size_t)sp * kFp8TokenBytes + 512 : 0),
+            cp_async_16_zfill(S + kChunkKV + half_off + 3072 + lane * 16,
+                              tok + (okk ? (size_t)sp * kFp8TokenBytes + 512 : 0),
                               okk ? 16 : 0);
           }
 #pragma unroll

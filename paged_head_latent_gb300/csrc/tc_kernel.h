@@ -11,7 +11,7 @@ namespace mla {
 struct TmaMaps {
   CUtensorMap ckv;  // [slots, 512], box 64 x 64, 128-byte swizzle (a whole run of 64 slots)
   CUtensorMap kpe;  // [slots, 64],  box 32 x 64, 64-byte swizzle (half of the positional dims)
-  // FP8 cache as [slots, 656] bytes: latent boxes 256 B x 16 tokens, scale boxes
+  // FP8 cache as [slots, 656] bytes: latent boxes 128 B x 64 tokens, scale boxes
   // 16 B x 32 tokens, rope boxes 64 B x 64 tokens (64-byte swizzle).
   CUtensorMap f8_lat;
   CUtensorMap f8_scl;
