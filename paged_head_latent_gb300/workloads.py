@@ -370,6 +370,12 @@ def prefill_causal_h128() -> Workload:
                         page_size=64, seed=1005, name="prefill_causal_h128")
 
 
+def prefill_causal_h128_r1() -> Workload:
+    """One request of the causal prefill batch, reduced for single-launch profiling: q_len
+    2048 after a prefix of 1024, 128 heads, page 64."""
+    return make_prefill([2048], [1024], num_qo_heads=128, page_size=64, seed=1015, name="prefill_causal_h128_r1")
+
+
 def mtp_b64_h16_q4_ps64() -> Workload:
     """Packed multi-token decode: batch 64, 16 heads, 4 tokens per request (64 rows per
     tile), page 64, kv lens uniform in [1024, 8192]."""
@@ -424,6 +430,7 @@ NAMED = {
     "decode_b128_h128_ps1": decode_b128_h128_ps1,
     "decode_b32_h128_skew": decode_b32_h128_skew,
     "prefill_causal_h128": prefill_causal_h128,
+    "prefill_causal_h128_r1": prefill_causal_h128_r1,
     "mtp_b64_h16_q4_ps64": mtp_b64_h16_q4_ps64,
     "sparse_b64_h128_topk2048": sparse_b64_h128_topk2048,
     "fp8_b64_h128_ps64": fp8_b64_h128_ps64,
