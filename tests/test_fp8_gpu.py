@@ -57,6 +57,32 @@ def test_fp8_decode_small(lib, page_size, heads):
         assert torch.equal(out, o2) and torch.equal(lse, l2)
 
 
+@pytest.mark.parametrize("page_size,heads", [(32, 100), (1, 1), (64, 33)])
+def test_fp8_decode_odd_shapes(lib, page_size, heads):
+    require_gpu()
+    lens = [2, 77, 640, 129, 1]
+    w = wl.quantize_fp8(wl.make_decode(lens, heads, page_size, seed=6400 + page_size + heads))
+    ref_out, ref_lse = oracle_run(w)
+    out, lse = lib.run_workload(w.to("cuda"))
+    torch.cuda.synchronize()
+    _close(out, lse, ref_out, ref_lse, f"fp8 ps{page_size} h{heads}")
+
+
+@pytest.mark.parametrize("workers", [1, 3, 40])
+def test_fp8_split_counts(lib, workers):
+    """Split rows (and, with one worker, one worker walking every tile through the FP8
+    producer's staging ring many times over)."""
+    require_gpu()
+    w = wl.quantize_fp8(wl.make_decode([3000, 65, 1999, 700], 128, 64, seed=6500 + workers))
+    ref_out, ref_lse = oracle_run(w)
+    wd = w.to("cuda")
+    ws = torch.zeros(lib.workload_workspace_bytes(wd, workers), dtype=torch.uint8, device="cuda")
+    out, lse = lib.run_workload(wd, workspace=ws, num_workers=workers)
+    torch.cuda.synchronize()
+    assert lib.read_device_status(ws) == 0
+    _close(out, lse, ref_out, ref_lse, f"fp8 workers={workers}")
+
+
 def test_fp8_full_size_every_element(lib):
     require_gpu()
     w = wl.by_name("fp8_b64_h128_ps64")
