@@ -38,7 +38,7 @@
 // 4 KB of kpe in 64-byte swizzle per stage), two partial-S exchange buffers (2 x 24 KB)
 // that the peer fills, and small reduction buffers.
 //
-// Warp roles (352 threads per CTA):
+// Warp roles (384 threads per CTA; 352 in the instance for packed tokens on whole pages):
 //   warps 0-7  softmax / correction / epilogue / Q loading.  Warp w serves TMEM lanes
 //              32*(w%4) .. +31 (lane = query head) and key columns 32*(w/4) .. +31 of
 //              each tile; the two warps of a lane group combine their row maxima through
@@ -53,6 +53,8 @@
 //   warp 9     issues S = Q.K^T (one thread) and owns TMEM
 //   warp 10    issues O += P.V (one thread); tcgen05.mma issue blocks while the tensor
 //              pipe is busy, so the two products get separate issuing threads.
+//   warp 11    second copy warp of the small-page and FP8 instances (each copy warp
+//              takes 32 of a tile's 64 keys); idle in the whole-page instance.
 #include <mutex>
 
 #include "common.cuh"
