@@ -121,6 +121,16 @@ def test_decode_all_empty(lib):
     check_full(lib, w)
 
 
+@pytest.mark.parametrize("batch,ps,workers", [(3000, 16, 0), (5000, 1, 7), (1500, 64, 150)])
+def test_decode_many_requests(lib, batch, ps, workers):
+    """Thousands of short requests (many rows per worker, most of them whole, some empty):
+    the on-device plan walks every request's length and every worker's range."""
+    gen = torch.Generator().manual_seed(2210 + batch)
+    lens = torch.randint(0, 150, (batch,), generator=gen).tolist()
+    w = wl.make_decode(lens, num_qo_heads=16, page_size=ps, seed=2210 + batch)
+    check_full(lib, w, num_workers=workers)
+
+
 def test_decode_nan_in_unreferenced_slots(lib):
     w = wl.make_decode([1, 63, 65, 200, 5], num_qo_heads=128, page_size=64, seed=2203, pool_pages=12)
     ref_out, ref_lse = oracle_run(w)
