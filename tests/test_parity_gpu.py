@@ -131,6 +131,20 @@ def test_decode_many_requests(lib, batch, ps, workers):
     check_full(lib, w, num_workers=workers)
 
 
+@pytest.mark.parametrize("ps", [64, 1])
+def test_decode_duplicate_slots(lib, ps):
+    """A slot listed twice in a request is two keys (the CSR reading): a duplicate inside a
+    64-slot run turns a whole-page tile into a copied one, and one request lists the same
+    slot many times."""
+    w = wl.make_decode([200, 130, 70], num_qo_heads=64, page_size=ps, seed=2220 + ps)
+    idx = w.kv_indices.clone()
+    ip = w.kv_indptr.tolist()
+    idx[ip[0] + 5] = idx[ip[0] + 3]
+    idx[ip[0] + 100] = idx[ip[0] + 150]
+    idx[ip[2]:ip[2] + 40] = idx[ip[2]]
+    check_full(lib, dataclasses.replace(w, kv_indices=idx))
+
+
 def test_decode_nan_in_unreferenced_slots(lib):
     w = wl.make_decode([1, 63, 65, 200, 5], num_qo_heads=128, page_size=64, seed=2203, pool_pages=12)
     ref_out, ref_lse = oracle_run(w)
